@@ -1,0 +1,351 @@
+#!/usr/bin/env python
+"""Benchmark of the INT8 convrot linear on one GB300 (or N, one process each).
+
+One step is one pass of the whole hot path over one batch: pack the
+activations (rotate + row absmax + quantize, one kernel) and run the linear
+(integer GEMM + fused scale/bias epilogue, one kernel) for the DiT MLP
+up-projection M=4096, K=3072, N=12288, G=256. Weights are quantized once,
+offline, before timing (the page "INT8 Convrot Safetensors" stores them
+quantized). Inputs are seeded synthetic tensors resident in HBM.
+
+Prints one JSON line (rank 0). ``--impl reference`` times the oracle (the
+plain fp64 CPU statement of the layer) on the host cores instead.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "convrot linear INT8 TOPS + pack GB/s at 4096x3072x12288, % of roofline"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="mlp_up")
+    ap.add_argument("--codes", choices=["auto", "i8", "bf16"], default="auto")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="approximate CPU time budget of the oracle baseline sample")
+    return ap.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.file, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        rows = []
+        with open(self.file.name) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                if self.uuid and parts[0] != self.uuid:
+                    continue
+                rows.append(parts)
+        os.unlink(self.file.name)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- CPU baseline (the oracle)
+def oracle_sample_run(wl, rows: int, Qw, sw, X, b):
+    """One oracle pass over `rows` rows of the workload: pack, integer GEMM, reconstruct."""
+    import oracle
+
+    Xs = X[:rows]
+    Qx, sx, _ = oracle.pack_rows(Xs, wl.G, want_pre_round=False)
+    A = oracle.gemm_i32(Qx, Qw, wl.k)
+    oracle.reconstruct(A, sx, sw, b)
+
+
+def cpu_baseline(wl, budget_s: float, steps: int = 1, warmup: int = 0):
+    """Times the oracle as it stands on this host's cores on a bounded row sample."""
+    import oracle
+    from int8_hadamard_rotated_convrot_gb300 import inputs
+
+    oracle.build()
+    X = inputs.activations(wl, rows=slice(0, min(wl.m, 512)))
+    W, b = inputs.weights(wl), inputs.bias(wl)
+    Qw, sw, _ = oracle.pack_rows(W, wl.G, want_pre_round=False)  # offline, untimed
+    per_row, trial = 1.0, 2
+    for _ in range(2):  # calibrate on a small, then a larger trial
+        t0 = time.perf_counter()
+        oracle_sample_run(wl, trial, Qw, sw, X, b)
+        per_row = max((time.perf_counter() - t0) / trial, 1e-6)
+        trial = int(max(2, min(X.shape[0], 0.2 * budget_s / max(steps, 1) / per_row)))
+    rows = int(max(2, min(X.shape[0], budget_s / max(steps, 1) / per_row)))
+    for _ in range(warmup):
+        oracle_sample_run(wl, rows, Qw, sw, X, b)
+    times = []
+    for _ in range(steps):
+        t0 = time.perf_counter()
+        oracle_sample_run(wl, rows, Qw, sw, X, b)
+        times.append(time.perf_counter() - t0)
+    t = sum(times) / len(times)
+    ops = 2.0 * rows * wl.n * wl.k
+    return {"value": ops / t / 1e12, "unit": "TOPS", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{rows} of {wl.m} rows of {wl.name} (pack + int GEMM vs all {wl.n} weight rows "
+                      f"+ reconstruct), fp64 oracle, {len(times)} step(s) of {t:.2f} s",
+            "seconds_per_step": t}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    from int8_hadamard_rotated_convrot_gb300 import inputs
+
+    wl = inputs.WORKLOADS[args.workload]
+    budget = max(1.0, min(args.cpu_seconds, 120.0 / max(args.steps + args.warmup, 1)))
+    cb = cpu_baseline(wl, budget * (args.steps), steps=args.steps, warmup=args.warmup)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": cb["value"], "unit": "TOPS", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": cb["seconds_per_step"] * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": f"{wl.name} M{wl.m} K{wl.k} N{wl.n} G{wl.G}",
+                   "sample": cb["sample"]},
+        "cpu_baseline": {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")},
+        "e2e": {"value": cb["value"], "unit": "TOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- GPU arm
+def run_ours(args):
+    import torch
+
+    rank, world, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (no CPU fallback)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+
+    from int8_hadamard_rotated_convrot_gb300 import build, inputs
+    from int8_hadamard_rotated_convrot_gb300 import convrot as cr
+
+    build.build()
+    cr.load()
+    wl = inputs.WORKLOADS[args.workload]
+    codes = {"i8": cr.CODES_I8, "bf16": cr.CODES_BF16, "auto": cr.CODES_I8}[args.codes]
+
+    # inputs: every rank runs the full workload on its own GPU (weak scaling; rows are independent)
+    X = torch.from_numpy(inputs.activations(wl)).to(dev)
+    W = torch.from_numpy(inputs.weights(wl)).to(dev)
+    b = torch.from_numpy(inputs.bias(wl)).to(dev)
+    touched = wl.m * wl.k * 4 + wl.n * wl.k * (1 if codes == cr.CODES_I8 else 2) + wl.m * wl.n * 4
+    R = max(2, -(-3 * L2_BYTES // touched) + 1)  # rotating sets so a reuse is > 2 L2s away
+    R = min(R, 6)
+    Xs = [X] + [X.clone() for _ in range(R - 1)]
+    pws = [cr.convrot_quantize_weights(W, wl.G, codes) for _ in range(R)]
+    pxs = [cr.empty_packed(wl.m, wl.k, codes, dev) for _ in range(R)]
+    Ys = [torch.empty((wl.m, wl.n), dtype=torch.float32, device=dev) for _ in range(R)]
+    del W
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i, ev=None):
+        j = i % R
+        if ev is not None:
+            ev[0].record(stream)
+        cr.convrot_pack_activations(Xs[j], wl.G, codes, out=pxs[j], stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        cr.convrot_linear(pxs[j], pws[j], b, out=Ys[j], stream=stream)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize(dev)
+
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        uuid = None
+    clocks = ClockSampler(uuid)
+    clocks.start()
+    time.sleep(0.3)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    # the timed loop runs several times over so the clock sampler sees a loaded GPU
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(i, evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize(dev)
+    total_ms = t_start.elapsed_time(t_end)
+    pack_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    gemm_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    # keep the GPU busy a little longer with the same steps for the clock record
+    t_keep = time.time()
+    i = 0
+    while time.time() - t_keep < 1.0:
+        step(i)
+        i += 1
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+
+    # end to end through the public API: pinned host X in, pinned host Y out, every step
+    e2e_steps = max(3, min(args.steps, 10))
+    Xh = torch.from_numpy(inputs.activations(wl)).pin_memory()
+    Yh = torch.empty((wl.m, wl.n), dtype=torch.float32).pin_memory()
+    Xd = torch.empty_like(Xs[0])
+
+    def e2e_step():
+        Xd.copy_(Xh, non_blocking=True)
+        cr.convrot_pack_activations(Xd, wl.G, codes, out=pxs[0], stream=stream)
+        cr.convrot_linear(pxs[0], pws[0], b, out=Ys[0], stream=stream)
+        Yh.copy_(Ys[0], non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+
+    ms_step = total_ms / args.steps
+    if pg:
+        t = torch.tensor([ms_step, e2e_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms_step, e2e_ms = float(t[0]), float(t[1])
+
+    ops = float(wl.int_ops)
+    value = world * ops / (ms_step * 1e-3) / 1e12
+    gemm_avg = sum(gemm_ms) / len(gemm_ms)
+    pack_avg = sum(pack_ms) / len(pack_ms)
+    pk = peaks()
+    gemm_tops = ops / (gemm_avg * 1e-3) / 1e12
+    pack_bytes = wl.m * (4 * wl.k + (1 if codes == cr.CODES_I8 else 2) * wl.k + 4)
+    pack_gbs = pack_bytes / (pack_avg * 1e-3) / 1e9
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tpath):
+        tr = json.load(open(tpath)).get(f"{wl.name}/{'i8' if codes == cr.CODES_I8 else 'bf16'}", {})
+        traffic = tr.get("gemm_bytes")
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": "TOPS", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "s8" if codes == cr.CODES_I8 else "bf16-coded s8",
+        "data": "synthetic (seeded N(0,1) activations with 0.1% outlier channels x50, N(0,0.02^2) weights)",
+        "config": {"workload": f"{wl.name} M{wl.m} K{wl.k} N{wl.n} G{wl.G}", "global_batch": wl.m * world,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "codes": "i8" if codes == cr.CODES_I8 else "bf16",
+                   "l2": f"{R} rotating input/output sets, {touched / 1e6:.0f} MB touched per step (> L2)"},
+        "pack_gbs": pack_gbs, "pack_ms": pack_avg, "gemm_ms": gemm_avg, "gemm_tops": gemm_tops,
+        "roofline": {"bound": "tensor", "achieved": gemm_tops, "peak": pk["bf16_tflops"],
+                     "unit": "TFLOP/s", "frac": gemm_tops / pk["bf16_tflops"], "traffic": traffic,
+                     "kernel": "gemm", "peak_source": f"{pk['source']} dense bf16 burst"},
+        "roofline_pack": {"bound": "hbm", "achieved": pack_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                          "frac": pack_gbs / pk["hbm_gbs"], "bytes_per_launch": pack_bytes,
+                          "peak_source": f"{pk['source']} copy bandwidth"},
+        "e2e": {"value": world * ops / (e2e_ms * 1e-3) / 1e12, "unit": "TOPS",
+                "h2d_bytes_per_step": wl.m * wl.k * 4, "d2h_bytes_per_step": wl.m * wl.n * 4,
+                "ms_per_step": e2e_ms},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        cb = cpu_baseline(wl, args.cpu_seconds)
+        line["cpu_baseline"] = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")}
+    print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

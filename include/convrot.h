@@ -1,0 +1,158 @@
+/*
+ * convrot.h -- C ABI of libconvrot, the GB300 (sm_103a) INT8 convrot linear.
+ *
+ * The layer is the one defined on the page "INT8 Convrot Safetensors"
+ * (stable-diffusion.cpp docs, int8_convrot.md):
+ *
+ *   X_rot = X R            R = block-diagonal normalized Kronecker power of
+ *                          H4, one block per contiguous group of G = 4^n
+ *                          input features ("How INT8 convrot works")
+ *   s_x[r] = max_i |X_rot[r, i]| / 127
+ *   Q_x[r, i] = clamp(round(X_rot[r, i] / s_x[r]), -127, 127)
+ *                          ("Runtime activation quantization"; weights use the
+ *                          same formulas offline, "Weight quantization")
+ *   A[r, o] = sum_i Q_x[r, i] * Q_w[o, i]      (signed 32-bit)
+ *   Y[r, o] = A[r, o] * s_x[r] * s_w[o] + b[o]
+ *
+ * "round" is round half away from zero. A row whose rotated values are all
+ * zero gets scale 0 and codes 0 (so its outputs are the bias).
+ *
+ * Conventions for every entry point:
+ *   - All tensor arguments are DEVICE pointers unless stated otherwise, in
+ *     row-major layout with the given leading dimension (in elements).
+ *   - The caller owns every buffer. The library never allocates, frees or
+ *     synchronizes; all work is enqueued on `stream` (0 = legacy default).
+ *   - Arguments are validated on the host before anything is enqueued; a
+ *     non-OK status means nothing was launched.
+ *   - CONVROT_ERR_CUDA means a launch failed; the CUDA error is left for the
+ *     caller to query (cudaGetLastError / cudaPeekAtLastError).
+ *   - Inputs must not alias outputs. Results are deterministic.
+ *   - Inputs must be finite; NaN or Inf inputs give unspecified codes.
+ */
+#ifndef CONVROT_H_
+#define CONVROT_H_
+
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    CONVROT_OK = 0,
+    CONVROT_ERR_INVALID_ARG = 1, /* null pointer, negative size, ld too small, mismatched operands */
+    CONVROT_ERR_GROUP_SIZE = 2,  /* G not 4^n (n >= 1), G does not divide k, or G > 4096 */
+    CONVROT_ERR_ALIGNMENT = 3,   /* a pointer or leading dimension breaks the alignment rules */
+    CONVROT_ERR_K_RANGE = 4,     /* k < 1 or k > CONVROT_MAX_K */
+    CONVROT_ERR_CUDA = 5,        /* a kernel launch failed */
+    CONVROT_ERR_TIMEOUT = 6,     /* written to *dev_status by a kernel whose bounded wait ran out */
+    CONVROT_ERR_UNSUPPORTED = 7  /* valid request this build has no kernel for */
+} convrot_status;
+
+/* Largest k: 127 * 127 * k must fit in a signed 32-bit accumulator ("Runtime
+ * activation quantization" accumulates in signed 32-bit integers). */
+#define CONVROT_MAX_K 133144
+
+/* Largest group size the pack kernel supports (4^6). */
+#define CONVROT_MAX_GROUP 4096
+
+/* Element type of the stored codes. Both hold the same integers in
+ * [-127, 127]; BF16 represents every one of them exactly and is the operand
+ * type the tensor-core GEMM reads directly. */
+typedef enum {
+    CONVROT_CODES_I8 = 0,
+    CONVROT_CODES_BF16 = 1
+} convrot_codes;
+
+/*
+ * A packed, rotated and quantized row block: the page's "packed runtime
+ * activation tensor" (I8 rows plus one floating-point scale per row,
+ * "Runtime activation quantization"), and equally a quantized weight (Q_w,
+ * s_w; "Weight quantization" stores one scale per output row, 1-D).
+ * Linears that share an input and G reuse one packed activation.
+ *
+ *   q          device, [rows, ldq] codes of type `codes`; columns k..kpad-1
+ *              (kpad = convrot_ldq(k)) are zero, columns past kpad are
+ *              neither read nor written. 16-byte aligned.
+ *   scale      device, [rows] fp32, 4-byte aligned.
+ *   rows, k    logical shape.
+ *   ldq        row pitch in elements; ldq >= convrot_ldq(k) and ldq % 16 == 0.
+ *   group_size G it was rotated with.
+ *   codes      a convrot_codes value.
+ *
+ * The pack functions read ldq, codes, q and scale from *out and fill rows,
+ * k and group_size.
+ */
+typedef struct {
+    void *q;
+    float *scale;
+    int64_t rows;
+    int64_t k;
+    int64_t ldq;
+    int32_t group_size;
+    int32_t codes;
+} convrot_packed;
+
+/* Padded code row length the GEMM reads: k rounded up to a multiple of 128. */
+int64_t convrot_ldq(int64_t k);
+
+/*
+ * Offline weight quantization ("Weight quantization"): W_rot = W R,
+ * s_w[o] = max_i |W_rot[o, i]| / 127, Q_w = clamp(round(W_rot / s_w), +-127).
+ *   W      device fp32 [n, ldw], 16-byte aligned, ldw >= k, ldw % 4 == 0.
+ *   n      output features (rows of W), n >= 0 (0: nothing is launched).
+ *   k      input features, 1 <= k <= CONVROT_MAX_K.
+ *   G      4^m with m >= 1, G | k, G <= CONVROT_MAX_GROUP.
+ *   out_w  caller-filled q/scale/ldq/codes; receives rows = n, k, G.
+ * Same kernel as convrot_pack_activations.
+ */
+convrot_status convrot_quantize_weights(const float *W, int64_t n, int64_t k, int64_t ldw,
+                                        int32_t G, convrot_packed *out_w, cudaStream_t stream);
+
+/*
+ * Runtime activation pack ("Runtime activation quantization"): rotate each
+ * row of X group-wise, take one absmax scale over the whole rotated row, and
+ * write the codes and the scale. One fused kernel: X is read once.
+ *   X      device fp32 [m, ldx], 16-byte aligned, ldx >= k, ldx % 4 == 0.
+ *   m      rows (tokens), m >= 0 (0: nothing is launched).
+ *   k, G   as for convrot_quantize_weights.
+ *   out_x  caller-filled q/scale/ldq/codes; receives rows = m, k, G.
+ */
+convrot_status convrot_pack_activations(const float *X, int64_t m, int64_t k, int64_t ldx,
+                                        int32_t G, convrot_packed *out_x, cudaStream_t stream);
+
+/*
+ * The linear: A = Q_x Q_w^T in exact integer arithmetic, then
+ * Y[r, o] = A[r, o] * s_x[r] * s_w[o] + b[o] in fp32 ("Runtime activation
+ * quantization"), fused into the GEMM's epilogue.
+ *   x          packed activations (m = x->rows).
+ *   w          packed weights (n = w->rows); same k, group_size and codes as x.
+ *   bias       device fp32 [n], or NULL for no bias.
+ *   Y          device fp32 [m, ldy], 16-byte aligned, ldy >= n, ldy % 4 == 0.
+ *   dev_status device int32 or NULL. A kernel that gives up a bounded wait
+ *              writes CONVROT_ERR_TIMEOUT there (read it after synchronizing);
+ *              it is never written otherwise, so the caller zeroes it first.
+ * m == 0 or n == 0 launches nothing.
+ */
+convrot_status convrot_linear(const convrot_packed *x, const convrot_packed *w, const float *bias,
+                              float *Y, int64_t ldy, int32_t *dev_status, cudaStream_t stream);
+
+/*
+ * The integer GEMM alone: A[r, o] = sum_i Q_x[r, i] * Q_w[o, i] as int32, for
+ * checking the accumulation bit for bit. Same operand rules as
+ * convrot_linear.
+ *   A      device int32 [m, lda], 16-byte aligned, lda >= n, lda % 4 == 0.
+ */
+convrot_status convrot_gemm_i32(const convrot_packed *x, const convrot_packed *w, int32_t *A,
+                                int64_t lda, int32_t *dev_status, cudaStream_t stream);
+
+/* Static, NUL-terminated description of a status. Never NULL. */
+const char *convrot_status_string(convrot_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CONVROT_H_ */

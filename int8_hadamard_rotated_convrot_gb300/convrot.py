@@ -1,0 +1,210 @@
+"""Python binding of libconvrot's C ABI (ctypes; argument marshalling only).
+
+The names mirror ``include/convrot.h``. Every step of the layer runs in the
+library's CUDA kernels; this module only turns torch CUDA tensors into device
+pointers and the current torch stream into a ``cudaStream_t``. There is no
+fallback: if the library is missing, calls raise.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from dataclasses import dataclass
+
+import torch
+
+from . import build as _build
+
+OK, ERR_INVALID_ARG, ERR_GROUP_SIZE, ERR_ALIGNMENT, ERR_K_RANGE, ERR_CUDA, ERR_TIMEOUT, ERR_UNSUPPORTED = range(8)
+CODES_I8, CODES_BF16 = 0, 1
+MAX_K = 133144
+MAX_GROUP = 4096
+
+EXPORTED = [
+    "convrot_ldq",
+    "convrot_quantize_weights",
+    "convrot_pack_activations",
+    "convrot_linear",
+    "convrot_gemm_i32",
+    "convrot_status_string",
+]
+
+
+class ConvrotError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+
+
+class _Packed(ctypes.Structure):
+    _fields_ = [
+        ("q", ctypes.c_void_p),
+        ("scale", ctypes.c_void_p),
+        ("rows", ctypes.c_int64),
+        ("k", ctypes.c_int64),
+        ("ldq", ctypes.c_int64),
+        ("group_size", ctypes.c_int32),
+        ("codes", ctypes.c_int32),
+    ]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load() -> ctypes.CDLL:
+    """Loads libconvrot.so (built in-tree by ``build.build()``); raises if absent."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB
+        if not os.path.exists(path):
+            raise RuntimeError(f"libconvrot.so is not built ({path}); run __graft_entry__.build()")
+        lib = ctypes.CDLL(path)
+        i64, i32, vp = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p
+        P = ctypes.POINTER(_Packed)
+        lib.convrot_ldq.argtypes = [i64]
+        lib.convrot_ldq.restype = i64
+        lib.convrot_quantize_weights.argtypes = [vp, i64, i64, i64, i32, P, vp]
+        lib.convrot_quantize_weights.restype = ctypes.c_int
+        lib.convrot_pack_activations.argtypes = [vp, i64, i64, i64, i32, P, vp]
+        lib.convrot_pack_activations.restype = ctypes.c_int
+        lib.convrot_linear.argtypes = [P, P, vp, vp, i64, vp, vp]
+        lib.convrot_linear.restype = ctypes.c_int
+        lib.convrot_gemm_i32.argtypes = [P, P, vp, i64, vp, vp]
+        lib.convrot_gemm_i32.restype = ctypes.c_int
+        lib.convrot_status_string.argtypes = [ctypes.c_int]
+        lib.convrot_status_string.restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    return load().convrot_status_string(int(status)).decode()
+
+
+convrot_status_string = status_string
+
+
+def convrot_ldq(k: int) -> int:
+    return int(load().convrot_ldq(int(k)))
+
+
+@dataclass
+class Packed:
+    """Owner of a packed block: codes q [rows, ldq] and fp32 scale [rows] (torch CUDA tensors)."""
+
+    q: torch.Tensor
+    scale: torch.Tensor
+    rows: int
+    k: int
+    group_size: int
+    codes: int
+
+    @property
+    def ldq(self) -> int:
+        return self.q.stride(0)
+
+    def struct(self) -> _Packed:
+        return _Packed(self.q.data_ptr() if self.q.numel() else None,
+                       self.scale.data_ptr() if self.scale.numel() else None,
+                       self.rows, self.k, self.ldq, self.group_size, self.codes)
+
+    def codes_as_int8(self) -> torch.Tensor:
+        """[rows, k] int8 view of the codes (a copy for bf16 codes)."""
+        q = self.q[:, : self.k]
+        return q if self.codes == CODES_I8 else q.to(torch.int8)
+
+
+def empty_packed(rows: int, k: int, codes: int = CODES_I8, device=None) -> Packed:
+    """Allocates (with torch) the buffers a pack call fills."""
+    ldq = convrot_ldq(k)
+    dtype = torch.int8 if codes == CODES_I8 else torch.bfloat16
+    device = device or torch.device("cuda", torch.cuda.current_device())
+    q = torch.empty((rows, ldq), dtype=dtype, device=device)
+    s = torch.empty((rows,), dtype=torch.float32, device=device)
+    return Packed(q, s, rows, k, 0, codes)
+
+
+def _stream(stream) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _check(status: int, what: str):
+    if status != OK:
+        raise ConvrotError(status, what)
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None or t.numel() == 0 else t.data_ptr()
+
+
+def _pack(fn, X: torch.Tensor, G: int, codes: int, out: Packed | None, stream, what: str) -> Packed:
+    if X.dtype != torch.float32 or not X.is_cuda or X.dim() != 2 or X.stride(1) != 1:
+        raise TypeError("X must be a 2-D row-major float32 CUDA tensor")
+    rows, k = X.shape
+    out = out or empty_packed(rows, k, codes, X.device)
+    st = out.struct()
+    _check(fn(_ptr(X), rows, k, X.stride(0), int(G), ctypes.byref(st), _stream(stream)), what)
+    out.rows, out.k, out.group_size = int(st.rows), int(st.k), int(st.group_size)
+    return out
+
+
+def convrot_quantize_weights(W: torch.Tensor, G: int, codes: int = CODES_I8, out: Packed | None = None,
+                             stream=None) -> Packed:
+    """Offline: Q_w, s_w of W [n, k] fp32 (page section "Weight quantization")."""
+    return _pack(load().convrot_quantize_weights, W, G, codes, out, stream, "convrot_quantize_weights")
+
+
+def convrot_pack_activations(X: torch.Tensor, G: int, codes: int = CODES_I8, out: Packed | None = None,
+                             stream=None) -> Packed:
+    """Runtime: Q_x, s_x of X [m, k] fp32 (page section "Runtime activation quantization")."""
+    return _pack(load().convrot_pack_activations, X, G, codes, out, stream, "convrot_pack_activations")
+
+
+def convrot_linear(x: Packed, w: Packed, bias: torch.Tensor | None = None, out: torch.Tensor | None = None,
+                   dev_status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Y [m, n] fp32 = (Q_x Q_w^T) * s_x s_w + b."""
+    if out is None:
+        out = torch.empty((x.rows, w.rows), dtype=torch.float32, device=x.q.device)
+    if bias is not None and (bias.dtype != torch.float32 or not bias.is_cuda):
+        raise TypeError("bias must be a float32 CUDA tensor")
+    xs, ws = x.struct(), w.struct()
+    _check(load().convrot_linear(ctypes.byref(xs), ctypes.byref(ws), _ptr(bias), _ptr(out),
+                                 out.stride(0) if out.dim() == 2 else 0, _ptr(dev_status),
+                                 _stream(stream)), "convrot_linear")
+    return out
+
+
+def convrot_gemm_i32(x: Packed, w: Packed, out: torch.Tensor | None = None,
+                     dev_status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """A [m, n] int32 = Q_x Q_w^T."""
+    if out is None:
+        out = torch.empty((x.rows, w.rows), dtype=torch.int32, device=x.q.device)
+    xs, ws = x.struct(), w.struct()
+    _check(load().convrot_gemm_i32(ctypes.byref(xs), ctypes.byref(ws), _ptr(out),
+                                   out.stride(0) if out.dim() == 2 else 0, _ptr(dev_status),
+                                   _stream(stream)), "convrot_gemm_i32")
+    return out
+
+
+def packed_from_codes(q_int8: torch.Tensor, scale: torch.Tensor, group_size: int, codes: int = CODES_I8) -> Packed:
+    """Wraps externally produced codes (e.g. a checkpoint's I8 weight and its scales) as a Packed.
+
+    Copies into the padded layout the GEMM reads: [rows, convrot_ldq(k)], zero past k.
+    """
+    rows, k = q_int8.shape
+    p = empty_packed(rows, k, codes, q_int8.device)
+    p.q.zero_()
+    p.q[:, :k].copy_(q_int8 if codes == CODES_I8 else q_int8.to(torch.bfloat16))
+    p.scale.copy_(scale.reshape(-1).to(torch.float32))
+    p.group_size = int(group_size)
+    return p

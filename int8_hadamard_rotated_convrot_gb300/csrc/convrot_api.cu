@@ -1,0 +1,181 @@
+// C-ABI entry points of libconvrot: host-side validation, then launches.
+// The operations are those of the page "INT8 Convrot Safetensors"
+// (stable-diffusion.cpp docs); see include/convrot.h for the contract.
+#include <cstdint>
+
+#include "../../include/convrot.h"
+#include "internal.h"
+
+namespace {
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Returns n for G = 4^n (n >= 1, G <= CONVROT_MAX_GROUP), else -1.
+int log4_group(int64_t G)
+{
+    if (G < 4 || G > CONVROT_MAX_GROUP) return -1;
+    int n = 0;
+    while (G > 1) {
+        if (G & 3) return -1;
+        G >>= 2;
+        ++n;
+    }
+    return n;
+}
+
+convrot_status check_k_g(int64_t k, int32_t G, int *log4g)
+{
+    if (k < 1 || k > CONVROT_MAX_K) return CONVROT_ERR_K_RANGE;
+    const int n = log4_group(G);
+    // the group size must be a power of four dividing the input features ("Checkpoint format")
+    if (n < 0 || k % G != 0) return CONVROT_ERR_GROUP_SIZE;
+    *log4g = n;
+    return CONVROT_OK;
+}
+
+convrot_status check_packed_buffers(const convrot_packed *p, int64_t rows, int64_t k)
+{
+    if (!p) return CONVROT_ERR_INVALID_ARG;
+    if (p->codes != CONVROT_CODES_I8 && p->codes != CONVROT_CODES_BF16) return CONVROT_ERR_INVALID_ARG;
+    if (p->ldq < convrot_ldq(k)) return CONVROT_ERR_INVALID_ARG;
+    if (p->ldq % 16 != 0) return CONVROT_ERR_ALIGNMENT;
+    if (rows > 0) {
+        if (!p->q || !p->scale) return CONVROT_ERR_INVALID_ARG;
+        if (!aligned(p->q, 16) || !aligned(p->scale, 4)) return CONVROT_ERR_ALIGNMENT;
+    }
+    return CONVROT_OK;
+}
+
+convrot_status pack_rows(const float *X, int64_t rows, int64_t k, int64_t ld, int32_t G,
+                         convrot_packed *out, cudaStream_t stream)
+{
+    int log4g = 0;
+    if (rows < 0 || !out) return CONVROT_ERR_INVALID_ARG;
+    convrot_status st = check_k_g(k, G, &log4g);
+    if (st != CONVROT_OK) return st;
+    if (ld < k) return CONVROT_ERR_INVALID_ARG;
+    st = check_packed_buffers(out, rows, k);
+    if (st != CONVROT_OK) return st;
+    if (rows > 0) {
+        if (!X) return CONVROT_ERR_INVALID_ARG;
+        if (!aligned(X, 16) || ld % 4 != 0) return CONVROT_ERR_ALIGNMENT;
+    }
+    out->rows = rows;
+    out->k = k;
+    out->group_size = G;
+    if (rows == 0) return CONVROT_OK;
+    convrot::PackArgs a{};
+    a.x = X;
+    a.ldx = ld;
+    a.rows = rows;
+    a.k = static_cast<int32_t>(k);
+    a.log4g = log4g;
+    a.q = out->q;
+    a.ldq = out->ldq;
+    a.kpad = static_cast<int32_t>(convrot_ldq(k));
+    a.scale = out->scale;
+    a.bf16 = out->codes == CONVROT_CODES_BF16;
+    return convrot::launch_pack(a, stream) == cudaSuccess ? CONVROT_OK : CONVROT_ERR_CUDA;
+}
+
+convrot_status check_pair(const convrot_packed *x, const convrot_packed *w)
+{
+    if (!x || !w) return CONVROT_ERR_INVALID_ARG;
+    if (x->rows < 0 || w->rows < 0) return CONVROT_ERR_INVALID_ARG;
+    if (x->k != w->k) return CONVROT_ERR_INVALID_ARG;
+    // packed activations are reused only by linears with the same group size ("Runtime activation quantization")
+    if (x->group_size != w->group_size) return CONVROT_ERR_GROUP_SIZE;
+    if (x->codes != w->codes) return CONVROT_ERR_INVALID_ARG;
+    int log4g = 0;
+    convrot_status st = check_k_g(x->k, x->group_size, &log4g);
+    if (st != CONVROT_OK) return st;
+    st = check_packed_buffers(x, x->rows, x->k);
+    if (st != CONVROT_OK) return st;
+    return check_packed_buffers(w, w->rows, w->k);
+}
+
+convrot_status run_gemm(const convrot_packed *x, const convrot_packed *w, const float *bias, float *Y,
+                        int32_t *A, int64_t ld, int32_t *dev_status, cudaStream_t stream)
+{
+    convrot_status st = check_pair(x, w);
+    if (st != CONVROT_OK) return st;
+    const int64_t m = x->rows, n = w->rows;
+    if (ld < n) return CONVROT_ERR_INVALID_ARG;
+    if (m > 0 && n > 0) {
+        void *out = Y ? static_cast<void *>(Y) : static_cast<void *>(A);
+        if (!out) return CONVROT_ERR_INVALID_ARG;
+        if (!aligned(out, 16) || ld % 4 != 0) return CONVROT_ERR_ALIGNMENT;
+        if (bias && !aligned(bias, 4)) return CONVROT_ERR_ALIGNMENT;
+        if (dev_status && !aligned(dev_status, 4)) return CONVROT_ERR_ALIGNMENT;
+    } else {
+        return CONVROT_OK;
+    }
+    convrot::GemmArgs g{};
+    g.qx = x->q;
+    g.ldqx = x->ldq;
+    g.qw = w->q;
+    g.ldqw = w->ldq;
+    g.m = m;
+    g.n = n;
+    g.kpad = static_cast<int32_t>(convrot_ldq(x->k));
+    g.sx = x->scale;
+    g.sw = w->scale;
+    g.bias = bias;
+    g.y = Y;
+    g.a = A;
+    g.ldy = ld;
+    g.dev_status = dev_status;
+    cudaError_t e = x->codes == CONVROT_CODES_I8 ? convrot::launch_gemm_imma(g, stream)
+                                                 : convrot::launch_gemm_tc(g, stream);
+    if (e == cudaErrorNotSupported) return CONVROT_ERR_UNSUPPORTED;
+    return e == cudaSuccess ? CONVROT_OK : CONVROT_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int64_t convrot_ldq(int64_t k) { return k <= 0 ? 0 : ((k + 127) / 128) * 128; }
+
+convrot_status convrot_quantize_weights(const float *W, int64_t n, int64_t k, int64_t ldw, int32_t G,
+                                        convrot_packed *out_w, cudaStream_t stream)
+{
+    return pack_rows(W, n, k, ldw, G, out_w, stream);
+}
+
+convrot_status convrot_pack_activations(const float *X, int64_t m, int64_t k, int64_t ldx, int32_t G,
+                                        convrot_packed *out_x, cudaStream_t stream)
+{
+    return pack_rows(X, m, k, ldx, G, out_x, stream);
+}
+
+convrot_status convrot_linear(const convrot_packed *x, const convrot_packed *w, const float *bias,
+                              float *Y, int64_t ldy, int32_t *dev_status, cudaStream_t stream)
+{
+    if (!Y && x && w && x->rows > 0 && w->rows > 0) return CONVROT_ERR_INVALID_ARG;
+    return run_gemm(x, w, bias, Y, nullptr, ldy, dev_status, stream);
+}
+
+convrot_status convrot_gemm_i32(const convrot_packed *x, const convrot_packed *w, int32_t *A,
+                                int64_t lda, int32_t *dev_status, cudaStream_t stream)
+{
+    if (!A && x && w && x->rows > 0 && w->rows > 0) return CONVROT_ERR_INVALID_ARG;
+    return run_gemm(x, w, nullptr, nullptr, A, lda, dev_status, stream);
+}
+
+const char *convrot_status_string(convrot_status s)
+{
+    switch (s) {
+    case CONVROT_OK: return "ok";
+    case CONVROT_ERR_INVALID_ARG: return "invalid argument";
+    case CONVROT_ERR_GROUP_SIZE: return "group size must be 4^n (n >= 1, at most 4096) and divide k";
+    case CONVROT_ERR_ALIGNMENT: return "pointer or leading dimension is not suitably aligned";
+    case CONVROT_ERR_K_RANGE: return "k must be in [1, 133144]";
+    case CONVROT_ERR_CUDA: return "CUDA launch failed";
+    case CONVROT_ERR_TIMEOUT: return "a kernel gave up a bounded wait";
+    case CONVROT_ERR_UNSUPPORTED: return "no kernel for this request in this build";
+    default: return "unknown status";
+    }
+}
+
+}  // extern "C"

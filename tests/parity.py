@@ -1,0 +1,67 @@
+"""Tolerance rules for comparing the CUDA path with the oracle.
+
+The rules (stated for the INT8 convrot linear, page "INT8 Convrot
+Safetensors", stable-diffusion.cpp docs):
+
+  - row scales: |s - s_ref| <= 1e-6 * s_ref;
+  - codes: at most ceil(1e-4 * count) entries differ from the oracle's, each
+    by exactly 1, and only where the oracle's fp64 pre-round value lies within
+    1e-4 of a .5 rounding boundary (the kernel rotates in fp32, the oracle in
+    fp64, so values that close to a boundary may round either way);
+  - given identical codes: the int32 accumulators are bit-exact, and
+    |Y - Y_ref| <= 1e-6 * (|A s_x s_w| + |b|) elementwise (Y_ref in fp64);
+  - end to end from X: max |Y - Y_ref| <= 1e-3 * max |Y_ref|.
+"""
+
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+S_RTOL = 1e-6
+CODE_FRAC = 1e-4
+BOUNDARY = 1e-4
+Y_RTOL_SAME_CODES = 1e-6
+Y_END_TO_END = 1e-3
+
+
+def check_scales(s_gpu: np.ndarray, s_ref: np.ndarray):
+    s_gpu = np.asarray(s_gpu, np.float64)
+    s_ref = np.asarray(s_ref, np.float64)
+    err = np.abs(s_gpu - s_ref)
+    bad = err > S_RTOL * np.abs(s_ref)
+    assert not bad.any(), (f"{bad.sum()} scales off; worst rel "
+                           f"{np.max(err / np.maximum(np.abs(s_ref), 1e-300)):.3e}")
+
+
+def check_codes(q_gpu: np.ndarray, q_ref: np.ndarray, pre_round: np.ndarray):
+    """q_gpu, q_ref: int [rows, k]; pre_round: the oracle's fp64 v = rot / s."""
+    q_gpu = np.asarray(q_gpu, np.int32)
+    q_ref = np.asarray(q_ref, np.int32)
+    diff = q_gpu != q_ref
+    n_diff = int(diff.sum())
+    if n_diff == 0:
+        return 0
+    assert n_diff <= math.ceil(CODE_FRAC * q_ref.size), f"{n_diff} of {q_ref.size} codes differ"
+    assert np.all(np.abs(q_gpu[diff] - q_ref[diff]) == 1), "a code differs by more than 1"
+    v = pre_round[diff]
+    dist = np.abs(np.abs(v - np.trunc(v)) - 0.5)
+    assert np.all(dist <= BOUNDARY), f"a differing code is {dist.max():.3e} from a .5 boundary"
+    return n_diff
+
+
+def check_y_same_codes(y_gpu: np.ndarray, y64_ref: np.ndarray, A: np.ndarray, sx, sw, bias):
+    base = np.abs(A.astype(np.float64) * np.asarray(sx, np.float64)[:, None]
+                  * np.asarray(sw, np.float64)[None, :])
+    if bias is not None:
+        base = base + np.abs(np.asarray(bias, np.float64))[None, :]
+    err = np.abs(np.asarray(y_gpu, np.float64) - y64_ref)
+    bad = err > Y_RTOL_SAME_CODES * base + 1e-30
+    assert not bad.any(), f"{bad.sum()} outputs off; worst {np.max(err / np.maximum(base, 1e-300)):.3e}"
+
+
+def check_y_end_to_end(y_gpu: np.ndarray, y_ref: np.ndarray):
+    err = np.max(np.abs(np.asarray(y_gpu, np.float64) - np.asarray(y_ref, np.float64)))
+    ref = np.max(np.abs(np.asarray(y_ref, np.float64)))
+    assert err <= Y_END_TO_END * ref, f"max|dY| = {err:.3e} > 1e-3 * {ref:.3e}"

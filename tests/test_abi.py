@@ -1,0 +1,150 @@
+"""CPU-side checks of the C ABI: the library builds, loads, exports every
+declared symbol, and rejects bad arguments on the host before launching.
+
+No call here reaches a kernel: each one either fails validation or has an
+empty problem (m == 0 or n == 0), which the ABI defines as a no-op.
+"""
+
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+from int8_hadamard_rotated_convrot_gb300 import build as cbuild
+from int8_hadamard_rotated_convrot_gb300 import convrot as cr
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+FAKE = 0x10000  # a 16-byte-aligned non-null address; never dereferenced on these paths
+
+
+@pytest.fixture(scope="module")
+def lib():
+    cbuild.build()
+    return cr.load()
+
+
+def declared_functions():
+    names = []
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"\b(convrot_\w+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert set(cr.EXPORTED) <= set(names) | {"convrot_status_string"}
+    for name in names:
+        assert hasattr(lib, name), name
+    # and the binding knows about all of them
+    assert set(names) <= set(cr.EXPORTED) | set(getattr(cr, "EXPORTED_EXTRA", []))
+
+
+def test_ldq(lib):
+    assert lib.convrot_ldq(1) == 128
+    assert lib.convrot_ldq(128) == 128
+    assert lib.convrot_ldq(129) == 256
+    assert lib.convrot_ldq(3072) == 3072
+    assert lib.convrot_ldq(0) == 0
+
+
+def test_status_strings(lib):
+    for s in range(8):
+        assert len(cr.status_string(s)) > 0
+    assert cr.status_string(999) == "unknown status"
+
+
+def packed(q=FAKE, scale=FAKE, ldq=128, codes=cr.CODES_I8, rows=0, k=0, G=0):
+    return cr._Packed(q, scale, rows, k, ldq, G, codes)
+
+
+def pack(lib, X=FAKE, m=4, k=256, ldx=256, G=256, out=None):
+    out = out or packed(ldq=cr.convrot_ldq(k) if k > 0 else 128)
+    return lib.convrot_pack_activations(X, m, k, ldx, G, ctypes.byref(out), None)
+
+
+@pytest.mark.parametrize("G", [1, 2, 8, 32, 128, 0, -4, 16384])
+def test_pack_rejects_bad_group(lib, G):
+    assert pack(lib, G=G) == cr.ERR_GROUP_SIZE
+
+
+def test_pack_rejects_group_not_dividing_k(lib):
+    assert pack(lib, k=96, ldx=96, G=64) == cr.ERR_GROUP_SIZE
+
+
+@pytest.mark.parametrize("k", [0, -1, 133148])
+def test_pack_rejects_k_range(lib, k):
+    assert pack(lib, k=k, ldx=max(k, 4), G=4) == cr.ERR_K_RANGE
+
+
+def test_pack_rejects_bad_pointers_and_lds(lib):
+    assert pack(lib, X=None) == cr.ERR_INVALID_ARG
+    assert pack(lib, X=FAKE + 4) == cr.ERR_ALIGNMENT
+    assert pack(lib, ldx=255) == cr.ERR_INVALID_ARG
+    assert pack(lib, k=256, ldx=258) == cr.ERR_ALIGNMENT
+    assert pack(lib, m=-1) == cr.ERR_INVALID_ARG
+    assert lib.convrot_pack_activations(FAKE, 4, 256, 256, 256, None, None) == cr.ERR_INVALID_ARG
+    assert pack(lib, out=packed(q=None)) == cr.ERR_INVALID_ARG
+    assert pack(lib, out=packed(scale=None)) == cr.ERR_INVALID_ARG
+    assert pack(lib, out=packed(q=FAKE + 8, ldq=256)) == cr.ERR_ALIGNMENT
+    assert pack(lib, out=packed(ldq=128)) == cr.ERR_INVALID_ARG  # ldq < convrot_ldq(256)
+    assert pack(lib, out=packed(ldq=264)) == cr.ERR_ALIGNMENT
+    assert pack(lib, out=packed(codes=2, ldq=256)) == cr.ERR_INVALID_ARG
+
+
+def test_pack_empty_is_noop_and_fills_shape(lib):
+    out = packed(q=None, scale=None, ldq=256)
+    assert lib.convrot_pack_activations(None, 0, 256, 256, 64, ctypes.byref(out), None) == cr.OK
+    assert (out.rows, out.k, out.group_size) == (0, 256, 64)
+    out = packed(q=None, scale=None, ldq=256)
+    assert lib.convrot_quantize_weights(None, 0, 192, 192, 64, ctypes.byref(out), None) == cr.OK
+
+
+def pair(mx=4, nw=4, k=256, G=256, codes=cr.CODES_I8):
+    ld = cr.convrot_ldq(k)
+    return (packed(rows=mx, k=k, G=G, ldq=ld, codes=codes), packed(rows=nw, k=k, G=G, ldq=ld, codes=codes))
+
+
+def linear(lib, x, w, Y=FAKE, ldy=64, bias=None, status=None):
+    return lib.convrot_linear(ctypes.byref(x), ctypes.byref(w), bias, Y, ldy, status, None)
+
+
+def test_linear_rejects_mismatches(lib):
+    x, w = pair()
+    w.k = 512
+    assert linear(lib, x, w) == cr.ERR_INVALID_ARG
+    x, w = pair()
+    w.group_size = 64
+    assert linear(lib, x, w) == cr.ERR_GROUP_SIZE
+    x, w = pair()
+    w.codes = cr.CODES_BF16
+    assert linear(lib, x, w) == cr.ERR_INVALID_ARG
+    x, w = pair(G=8)
+    assert linear(lib, x, w) == cr.ERR_GROUP_SIZE
+    x, w = pair()
+    assert linear(lib, x, w, ldy=2) == cr.ERR_INVALID_ARG
+    assert linear(lib, x, w, Y=None) == cr.ERR_INVALID_ARG
+    assert linear(lib, x, w, Y=FAKE + 4) == cr.ERR_ALIGNMENT
+    assert linear(lib, x, w, ldy=6) == cr.ERR_ALIGNMENT
+    assert linear(lib, x, w, bias=FAKE + 2) == cr.ERR_ALIGNMENT
+    x.q = None
+    assert linear(lib, x, w) == cr.ERR_INVALID_ARG
+    assert lib.convrot_linear(None, ctypes.byref(w), None, FAKE, 64, None, None) == cr.ERR_INVALID_ARG
+
+
+def test_linear_empty_is_noop(lib):
+    x, w = pair(mx=0)
+    assert linear(lib, x, w, Y=None) == cr.OK
+    x, w = pair(nw=0)
+    assert linear(lib, x, w, Y=None) == cr.OK
+
+
+def test_gemm_i32_validation(lib):
+    x, w = pair()
+    assert lib.convrot_gemm_i32(ctypes.byref(x), ctypes.byref(w), None, 4, None, None) == cr.ERR_INVALID_ARG
+    assert lib.convrot_gemm_i32(ctypes.byref(x), ctypes.byref(w), FAKE, 3, None, None) == cr.ERR_INVALID_ARG
+    x, w = pair(mx=0)
+    assert lib.convrot_gemm_i32(ctypes.byref(x), ctypes.byref(w), None, 4, None, None) == cr.OK

@@ -1,0 +1,261 @@
+"""GPU parity: the CUDA path through the C ABI against the oracle.
+
+Tolerances are those of tests/parity.py. Small cases compare every element;
+the full DiT-shaped workloads compare sampled rows the oracle can compute
+quickly, plus the ragged tail rows, in the launch configuration bench.py uses.
+"""
+
+import json
+import os
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+import oracle  # noqa: E402
+from int8_hadamard_rotated_convrot_gb300 import convrot as cr  # noqa: E402
+from int8_hadamard_rotated_convrot_gb300 import inputs  # noqa: E402
+
+from . import parity  # noqa: E402
+
+CODES = [cr.CODES_I8, cr.CODES_BF16]
+CODE_IDS = ["i8", "bf16"]
+GEMM_CODES = [cr.CODES_I8]
+GEMM_IDS = ["i8"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from int8_hadamard_rotated_convrot_gb300 import build
+
+    build.build()
+    cr.load()
+    yield
+    torch.cuda.synchronize()
+
+
+def to_dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def codes_np(p: cr.Packed) -> np.ndarray:
+    return p.codes_as_int8().cpu().numpy().astype(np.int32)
+
+
+def special_rows(rng, m, k):
+    X = rng.standard_normal((m, k)).astype(np.float32)
+    X[:, rng.choice(k, size=max(1, k // 1000), replace=False)] *= 50
+    X[0] = 0.0                      # zero row -> scale 0, codes 0
+    if m > 1:
+        X[1] = 0.0
+        X[1, k // 3] = 1e4          # one spike spread over its group
+    if m > 2:
+        X[2] = 0.75                 # constant row: rotation output is exact
+    if m > 3:
+        X[3] *= 1e20                # huge but finite
+    if m > 4:
+        X[4] *= 1e-20               # tiny
+    return X
+
+
+def gpu_pack(X_np, G, codes, ldx_extra=4, canary=True):
+    m, k = X_np.shape
+    ldx = k + ldx_extra
+    Xbig = np.zeros((m, ldx), np.float32)
+    Xbig[:, :k] = X_np
+    Xd = to_dev(Xbig)[:, :k]
+    ldq = cr.convrot_ldq(k) + (64 if canary else 0)
+    dtype = torch.int8 if codes == cr.CODES_I8 else torch.bfloat16
+    fill = 90 if codes == cr.CODES_I8 else 3.0
+    qbig = torch.full((m + 2, ldq), fill, dtype=dtype, device="cuda")
+    sbig = torch.full((m + 1,), -7.0, dtype=torch.float32, device="cuda")
+    out = cr.Packed(qbig[:m], sbig[:m], m, k, 0, codes)
+    cr.convrot_pack_activations(Xd, G, codes, out=out)
+    torch.cuda.synchronize()
+    kpad = cr.convrot_ldq(k)
+    # nothing outside [m, kpad) and the m scales was written; the pad is zero
+    assert torch.all(qbig[:m, kpad:] == fill)
+    assert torch.all(qbig[m:] == fill)
+    assert float(sbig[m]) == -7.0
+    assert torch.all(qbig[:m, k:kpad] == 0)
+    return out
+
+
+@pytest.mark.parametrize("codes", CODES, ids=CODE_IDS)
+@pytest.mark.parametrize("G,k", [(4, 3072), (16, 3072), (64, 3072), (256, 3072), (1024, 3072),
+                                 (4096, 8192), (16, 400), (64, 192), (4, 4), (256, 256)])
+def test_pack_matches_oracle(G, k, codes):
+    rng = np.random.default_rng(G * 7 + k)
+    m = 37
+    X = special_rows(rng, m, k)
+    p = gpu_pack(X, G, codes)
+    Q, s, v = oracle.pack_rows(X, G)
+    parity.check_scales(p.scale.cpu().numpy(), s)
+    parity.check_codes(codes_np(p), Q, v)
+    assert float(p.scale[0]) == 0.0 and torch.all(p.q[0] == 0)
+
+
+def test_pack_hand_worked_rows(golden_dir):
+    cases = json.load(open(os.path.join(golden_dir, "hand_worked_rows.json")))["rows"]
+    for c in cases:
+        for codes in CODES:
+            X = np.array([c["x"]], np.float32)
+            p = gpu_pack(X, c["G"], codes)
+            num, den = c["scale_over"]
+            assert float(p.scale[0]) == float(np.float32(num / den)), c["why"]
+            np.testing.assert_array_equal(codes_np(p)[0], np.array(c["Q"]), err_msg=c["why"])
+
+
+@pytest.mark.parametrize("G,k", [(256, 65536), (1024, 133120), (4, 131072), (4096, 131072)])
+def test_pack_long_rows_use_clusters(G, k):
+    rng = np.random.default_rng(k + G)
+    X = special_rows(rng, 3, k)
+    p = gpu_pack(X, G, cr.CODES_I8)
+    Q, s, v = oracle.pack_rows(X, G)
+    parity.check_scales(p.scale.cpu().numpy(), s)
+    parity.check_codes(codes_np(p), Q, v)
+
+
+def test_quantize_weights_equals_pack():
+    rng = np.random.default_rng(5)
+    W = (0.02 * rng.standard_normal((300, 512))).astype(np.float32)
+    Wd = to_dev(W)
+    a = cr.convrot_quantize_weights(Wd, 256)
+    b = cr.convrot_pack_activations(Wd, 256)
+    torch.cuda.synchronize()
+    assert torch.equal(a.q, b.q) and torch.equal(a.scale, b.scale)
+    Q, s, v = oracle.pack_rows(W, 256)
+    parity.check_scales(a.scale.cpu().numpy(), s)
+    parity.check_codes(codes_np(a), Q, v)
+
+
+def test_empty_pack_and_linear():
+    X = torch.empty((0, 256), dtype=torch.float32, device="cuda")
+    p = cr.convrot_pack_activations(X, 256)
+    w = cr.convrot_quantize_weights(torch.randn(8, 256, device="cuda"), 256)
+    Y = cr.convrot_linear(p, w)
+    torch.cuda.synchronize()
+    assert Y.shape == (0, 8)
+
+
+def random_codes(rng, rows, k, sat=False):
+    if sat:
+        return np.where(rng.random((rows, k)) < 0.5, -127, 127).astype(np.int8)
+    return rng.integers(-127, 128, size=(rows, k), dtype=np.int8)
+
+
+@pytest.mark.parametrize("codes", GEMM_CODES, ids=GEMM_IDS)
+@pytest.mark.parametrize("m,n,k,G", [(200, 300, 640, 64), (1, 1, 4, 4), (129, 257, 192, 64),
+                                     (256, 384, 3072, 256), (37, 1000, 1024, 1024)])
+def test_gemm_identical_codes_bit_exact(m, n, k, G, codes):
+    rng = np.random.default_rng(m * n + k)
+    Qx, Qw = random_codes(rng, m, k), random_codes(rng, n, k)
+    sx = rng.uniform(0.001, 1.0, m).astype(np.float32)
+    sw = rng.uniform(0.0001, 0.01, n).astype(np.float32)
+    sx[0] = 0.0
+    b = rng.standard_normal(n).astype(np.float32)
+    px = cr.packed_from_codes(to_dev(Qx), to_dev(sx), G, codes)
+    pw = cr.packed_from_codes(to_dev(Qw), to_dev(sw), G, codes)
+    A = cr.convrot_gemm_i32(px, pw)
+    Ybig = torch.full((m + 1, n + 4), -3.0, dtype=torch.float32, device="cuda")
+    Y = cr.convrot_linear(px, pw, to_dev(b), out=Ybig[:m, :n])
+    torch.cuda.synchronize()
+    A_ref = oracle.gemm_i32(Qx, Qw, k)
+    np.testing.assert_array_equal(A.cpu().numpy(), A_ref)
+    _, Y64 = oracle.reconstruct(A_ref, sx, sw, b)
+    parity.check_y_same_codes(Y.cpu().numpy(), Y64, A_ref, sx, sw, b)
+    assert torch.all(Ybig[m:] == -3.0) and torch.all(Ybig[:, n:] == -3.0)
+    # no bias
+    Y0 = cr.convrot_linear(px, pw)
+    torch.cuda.synchronize()
+    _, Y64n = oracle.reconstruct(A_ref, sx, sw, None)
+    parity.check_y_same_codes(Y0.cpu().numpy(), Y64n, A_ref, sx, sw, None)
+
+
+@pytest.mark.parametrize("codes", GEMM_CODES, ids=GEMM_IDS)
+def test_gemm_saturated_int32_headroom(codes):
+    """All-+-127 codes at k = 12288: |A| reaches 16129 * k = 198,193,152."""
+    rng = np.random.default_rng(1)
+    m, n, k = 130, 136, 12288
+    Qx = random_codes(rng, m, k, sat=True)
+    Qw = random_codes(rng, n, k, sat=True)
+    Qx[0] = 127
+    Qw[0] = 127
+    Qw[1] = -127
+    px = cr.packed_from_codes(to_dev(Qx), torch.ones(m, device="cuda"), 256, codes)
+    pw = cr.packed_from_codes(to_dev(Qw), torch.ones(n, device="cuda"), 256, codes)
+    A = cr.convrot_gemm_i32(px, pw).cpu().numpy()
+    A_ref = oracle.gemm_i32(Qx, Qw, k)
+    assert A_ref[0, 0] == 16129 * k and A_ref[0, 1] == -16129 * k
+    np.testing.assert_array_equal(A, A_ref)
+
+
+@pytest.mark.parametrize("codes", GEMM_CODES, ids=GEMM_IDS)
+def test_linear_end_to_end_tiny(codes):
+    wl = inputs.WORKLOADS["tiny"]
+    X, W, b = inputs.activations(wl), inputs.weights(wl), inputs.bias(wl)
+    px = cr.convrot_pack_activations(to_dev(X), wl.G, codes)
+    pw = cr.convrot_quantize_weights(to_dev(W), wl.G, codes)
+    Y = cr.convrot_linear(px, pw, to_dev(b))
+    A = cr.convrot_gemm_i32(px, pw)
+    torch.cuda.synchronize()
+    ref = oracle.linear(X, W, b, wl.G)
+    parity.check_scales(px.scale.cpu().numpy(), ref["sx"])
+    parity.check_scales(pw.scale.cpu().numpy(), ref["sw"])
+    parity.check_codes(codes_np(px), ref["Qx"], ref["vx"])
+    Qw_ref, _, vw = oracle.pack_rows(W, wl.G)
+    parity.check_codes(codes_np(pw), Qw_ref, vw)
+    parity.check_y_end_to_end(Y.cpu().numpy(), ref["Y64"])
+    # with the GPU's own codes the integer product and the epilogue are exact
+    qx, qw = codes_np(px).astype(np.int8), codes_np(pw).astype(np.int8)
+    A_ref = oracle.gemm_i32(qx, qw, wl.k)
+    np.testing.assert_array_equal(A.cpu().numpy(), A_ref)
+    sx, sw = px.scale.cpu().numpy(), pw.scale.cpu().numpy()
+    _, Y64 = oracle.reconstruct(A_ref, sx, sw, b)
+    parity.check_y_same_codes(Y.cpu().numpy(), Y64, A_ref, sx, sw, b)
+
+
+FULL = ["attn_qkv", "mlp_up", "mlp_down", "sweep_G4", "sweep_G16", "sweep_G64", "sweep_G1024",
+        "video_n13824"]
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_sampled(name):
+    """Full workload on the GPU in the bench's configuration; oracle on sampled rows."""
+    wl = inputs.WORKLOADS[name]
+    codes = GEMM_CODES[-1]
+    X, W, b = inputs.activations(wl), inputs.weights(wl), inputs.bias(wl)
+    px = cr.convrot_pack_activations(to_dev(X), wl.G, codes)
+    pw = cr.convrot_quantize_weights(to_dev(W), wl.G, codes)
+    Y = cr.convrot_linear(px, pw, to_dev(b))
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(123)
+    n_rows = 96 if wl.m * wl.n * wl.k > 2e12 else 128
+    rows = np.unique(np.concatenate([rng.choice(wl.m - 8, n_rows, replace=False),
+                                     np.arange(wl.m - 8, wl.m)]))
+    Xs = X[rows]
+    Qx_ref, sx_ref, vx = oracle.pack_rows(Xs, wl.G)
+    Qw_ref, sw_ref, vw = oracle.pack_rows(W, wl.G)
+    sx_gpu = px.scale.cpu().numpy()[rows]
+    qx_gpu = codes_np(px)[rows]
+    parity.check_scales(sx_gpu, sx_ref)
+    parity.check_codes(qx_gpu, Qx_ref, vx)
+    sw_gpu = pw.scale.cpu().numpy()
+    qw_gpu = codes_np(pw)
+    parity.check_scales(sw_gpu, sw_ref)
+    parity.check_codes(qw_gpu, Qw_ref, vw)
+    del vw
+    Y_rows = Y[torch.from_numpy(rows).cuda()].cpu().numpy()
+    # same codes: exact integer product, epilogue within 1e-6
+    A_gpu_codes = oracle.gemm_i32(qx_gpu.astype(np.int8), qw_gpu.astype(np.int8), wl.k)
+    _, Y64 = oracle.reconstruct(A_gpu_codes, sx_gpu, sw_gpu, b)
+    parity.check_y_same_codes(Y_rows, Y64, A_gpu_codes, sx_gpu, sw_gpu, b)
+    # end to end against the oracle's own codes
+    A_ref = oracle.gemm_i32(Qx_ref, Qw_ref, wl.k)
+    _, Y64_ref = oracle.reconstruct(A_ref, sx_ref, sw_ref, b)
+    parity.check_y_end_to_end(Y_rows, Y64_ref)
