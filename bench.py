@@ -127,7 +127,7 @@ def cpu_baseline(wl, budget_s: float, steps: int = 1, warmup: int = 0):
     from int8_hadamard_rotated_convrot_gb300 import inputs
 
     oracle.build()
-    X = inputs.activations(wl, rows=slice(0, min(wl.m, 512)))
+    X = inputs.activations(wl)
     W, b = inputs.weights(wl), inputs.bias(wl)
     Qw, sw, _ = oracle.pack_rows(W, wl.G, want_pre_round=False)  # offline, untimed
     per_row, trial = 1.0, 2

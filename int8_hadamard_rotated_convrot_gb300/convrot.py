@@ -147,6 +147,12 @@ def _ptr(t: torch.Tensor | None):
     return None if t is None or t.numel() == 0 else t.data_ptr()
 
 
+def _padded_out(m: int, n: int, dtype, device) -> torch.Tensor:
+    """[m, n] output whose row pitch is a multiple of 4 elements (16-byte rows), as the ABI asks."""
+    ld = (n + 3) // 4 * 4
+    return torch.empty((m, ld), dtype=dtype, device=device)[:, :n]
+
+
 def _pack(fn, X: torch.Tensor, G: int, codes: int, out: Packed | None, stream, what: str) -> Packed:
     if X.dtype != torch.float32 or not X.is_cuda or X.dim() != 2 or X.stride(1) != 1:
         raise TypeError("X must be a 2-D row-major float32 CUDA tensor")
@@ -174,7 +180,7 @@ def convrot_linear(x: Packed, w: Packed, bias: torch.Tensor | None = None, out: 
                    dev_status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """Y [m, n] fp32 = (Q_x Q_w^T) * s_x s_w + b."""
     if out is None:
-        out = torch.empty((x.rows, w.rows), dtype=torch.float32, device=x.q.device)
+        out = _padded_out(x.rows, w.rows, torch.float32, x.q.device)
     if bias is not None and (bias.dtype != torch.float32 or not bias.is_cuda):
         raise TypeError("bias must be a float32 CUDA tensor")
     xs, ws = x.struct(), w.struct()
@@ -188,7 +194,7 @@ def convrot_gemm_i32(x: Packed, w: Packed, out: torch.Tensor | None = None,
                      dev_status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """A [m, n] int32 = Q_x Q_w^T."""
     if out is None:
-        out = torch.empty((x.rows, w.rows), dtype=torch.int32, device=x.q.device)
+        out = _padded_out(x.rows, w.rows, torch.int32, x.q.device)
     xs, ws = x.struct(), w.struct()
     _check(load().convrot_gemm_i32(ctypes.byref(xs), ctypes.byref(ws), _ptr(out),
                                    out.stride(0) if out.dim() == 2 else 0, _ptr(dev_status),
