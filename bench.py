@@ -196,7 +196,7 @@ def run_ours(args):
     build.build()
     cr.load()
     wl = inputs.WORKLOADS[args.workload]
-    codes = {"i8": cr.CODES_I8, "bf16": cr.CODES_BF16, "auto": cr.CODES_I8}[args.codes]
+    codes = {"i8": cr.CODES_I8, "bf16": cr.CODES_BF16, "auto": cr.CODES_BF16}[args.codes]
 
     # inputs: every rank runs the full workload on its own GPU (weak scaling; rows are independent)
     X = torch.from_numpy(inputs.activations(wl)).to(dev)

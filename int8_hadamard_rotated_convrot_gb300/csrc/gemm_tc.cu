@@ -1,8 +1,465 @@
-// Placeholder until the tcgen05 GEMM lands: bf16-coded operands are rejected.
+// Exact integer GEMM on the 5th-generation tensor cores (tcgen05.mma,
+// kind::f16), with the reconstruction fused into the epilogue.
+//
+// Computes, from "Runtime activation quantization" on the page "INT8 Convrot
+// Safetensors" (stable-diffusion.cpp docs):
+//   A[r, o] = sum_i Q_x[r, i] * Q_w[o, i]            (exact, int32)
+//   Y[r, o] = A[r, o] * s_x[r] * s_w[o] + b[o]        (fp32)
+//
+// sm_103a has no integer kind for tcgen05.mma, so the int8 codes are carried
+// as bf16 (every integer in [-127, 127] is exact in bf16) and multiplied with
+// fp32 accumulation in tensor memory. Each product is an integer of magnitude
+// <= 16129, so any sum of at most 1024 of them stays below 2^24 and is exact
+// in fp32. The K loop therefore runs in chunks of 1024: each chunk
+// accumulates from zero in a TMEM buffer, and the epilogue warps convert the
+// chunk's (exact, integer-valued) fp32 sums to int32 and add them to int32
+// register accumulators. The result equals the page's signed 32-bit
+// accumulation bit for bit.
+//
+// Structure (one CTA per SM, persistent over 128 x 256 output tiles):
+//   warp 0      TMA producer: 64-wide K slices of A (128 rows) and B (256
+//               rows), 128-byte swizzled, into a 4-stage shared-memory ring.
+//   warp 1      allocates 512 TMEM columns (two 128 x 256 fp32 buffers) and
+//               issues tcgen05.mma (M = 128, N = 256, K = 16) from one thread.
+//   warps 2-9   epilogue: drain each finished chunk from TMEM (tcgen05.ld),
+//               accumulate in int32, and after the last chunk of a tile write
+//               Y (or the raw int32 A) while the MMA warp runs the next chunk
+//               into the other TMEM buffer.
+// Every mbarrier wait is bounded: a wait that runs out writes
+// CONVROT_ERR_TIMEOUT to the caller's status word and the CTA winds down
+// (in-flight copies and MMAs are waited for, TMEM is freed).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/convrot.h"
 #include "internal.h"
 
 namespace convrot {
+namespace {
 
-cudaError_t launch_gemm_tc(const GemmArgs &, cudaStream_t) { return cudaErrorNotSupported; }
+constexpr int BM = 128, BN = 256, BK = 64;  // BK bf16 = 128 B = one swizzle span
+constexpr int STAGES = 4;
+constexpr int UMMA_K = 16;
+constexpr int CHUNK_KSTAGES = 1024 / BK;  // K elements per exact fp32 chunk / BK
+constexpr int A_BYTES = BM * BK * 2;
+constexpr int B_BYTES = BN * BK * 2;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int EPI_WARPS = 8;
+constexpr int THREADS = 64 + EPI_WARPS * 32;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr int BAR_BYTES = 256;
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
+constexpr uint64_t kTimeoutNs = 4000000000ull;  // 4 s
+
+// instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major, M = 128, N = 256
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(BN >> 3) << 17) |
+                            (uint32_t(BM >> 4) << 24);
+
+__device__ __forceinline__ uint64_t globaltimer()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Waits for the phase with the given parity; false if it did not come within the limit.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    for (;;) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer() - t0 > kTimeoutNs) return false;
+    }
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
+                                            uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, "
+        "{%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr)
+{
+    return (uint64_t((addr >> 4) & 0x3fff)) | (uint64_t(1) << 16) | (uint64_t(1024 >> 4) << 32) |
+           (uint64_t(1) << 46) | (uint64_t(2) << 61);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(kIdesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+// 32 lanes x 32 consecutive 32-bit columns; thread i of the warp gets lane (base + i).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
+          "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
+          "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+struct TcParams {
+    int64_t m, n;
+    int32_t kstages;  // kpad / BK
+    const float *sx, *sw, *bias;
+    float *y;
+    int32_t *a;
+    int64_t ldy;
+    int32_t *dev_status;
+};
+
+template <bool kRawInt32>
+__global__ void __launch_bounds__(THREADS, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   TcParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = static_cast<uint32_t>(__cvta_generic_to_shared(smem_raw));
+    const uint32_t base = (raw + 1023u) & ~1023u;  // swizzle atoms need 1024-byte alignment
+    uint8_t *gbase = smem_raw + (base - raw);
+    const uint32_t bars = base + STAGES * STAGE_BYTES;
+    auto full_bar = [&](int s) { return bars + 8u * s; };
+    auto empty_bar = [&](int s) { return bars + 8u * (STAGES + s); };
+    auto accf_bar = [&](int b) { return bars + 8u * (2 * STAGES + b); };
+    auto acce_bar = [&](int b) { return bars + 8u * (2 * STAGES + 2 + b); };
+    const uint32_t done_bar = bars + 8u * (2 * STAGES + 4);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + STAGES * STAGE_BYTES + 128);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + STAGES * STAGE_BYTES + 132);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t n_mt = (p.m + BM - 1) / BM, n_nt = (p.n + BN - 1) / BN;
+    const int64_t n_tiles = n_mt * n_nt;
+    const int kst = p.kstages;
+    const int n_chunks = (kst + CHUNK_KSTAGES - 1) / CHUNK_KSTAGES;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(accf_bar(b), 1);
+            mbar_init(acce_bar(b), EPI_WARPS);
+        }
+        mbar_init(done_bar, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         static_cast<uint32_t>(__cvta_generic_to_shared(tmem_slot))),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    auto fail = [&]() {
+        *abort_flag = 1;
+        if (p.dev_status) atomicExch(p.dev_status, static_cast<int32_t>(CONVROT_ERR_TIMEOUT));
+    };
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int issued = 0;
+            bool ok = true;
+            for (int64_t t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+                const int mt = static_cast<int>(t % n_mt), nt = static_cast<int>(t / n_mt);
+                for (int ks = 0; ks < kst; ++ks) {
+                    if (*abort_flag || !mbar_wait(empty_bar(stage), phase ^ 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t sa = base + stage * STAGE_BYTES;
+                    mbar_arrive_expect_tx(full_bar(stage), STAGE_BYTES);
+                    tma_load_2d(sa, &tmA, ks * BK, mt * BM, full_bar(stage));
+                    tma_load_2d(sa + A_BYTES, &tmB, ks * BK, nt * BN, full_bar(stage));
+                    ++issued;
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                fail();
+                // let the copies already issued land before the CTA's shared memory goes away
+                for (int i = 0; i < STAGES && i < issued; ++i) {
+                    if (--stage < 0) {
+                        stage = STAGES - 1;
+                        phase ^= 1u;
+                    }
+                    mbar_wait(full_bar(stage), phase);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t chunk_iter = 0;
+            bool ok = true;
+            for (int64_t t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+                for (int c = 0; c < n_chunks && ok; ++c, ++chunk_iter) {
+                    const uint32_t buf = chunk_iter & 1u;
+                    if (*abort_flag || !mbar_wait(acce_bar(buf), ((chunk_iter >> 1) & 1u) ^ 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem_base + buf * BN;
+                    const int ks0 = c * CHUNK_KSTAGES;
+                    const int ks1 = ks0 + CHUNK_KSTAGES < kst ? ks0 + CHUNK_KSTAGES : kst;
+                    for (int ks = ks0; ks < ks1; ++ks) {
+                        if (*abort_flag || !mbar_wait(full_bar(stage), phase)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t sa = base + stage * STAGE_BYTES;
+                        const uint64_t da = smem_desc(sa), db = smem_desc(sa + A_BYTES);
+#pragma unroll
+                        for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+                            // +32 bytes along K inside the swizzle span per K = 16 step
+                            mma_bf16(d_tmem, da + 2u * kk, db + 2u * kk, (ks > ks0 || kk > 0) ? 1u : 0u);
+                        }
+                        mma_commit(empty_bar(stage));  // frees the stage once these MMAs finish
+                        if (++stage == STAGES) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
+                    if (!ok) break;
+                    mma_commit(accf_bar(buf));  // chunk finished: epilogue may drain it
+                }
+            }
+            if (!ok) fail();
+            // every MMA this thread issued has completed before TMEM is released
+            mma_commit(done_bar);
+            mbar_wait(done_bar, 0);
+        }
+        __syncwarp();
+    } else {
+        const int q = warp & 3;              // TMEM lane quadrant this warp may access
+        const int h = (warp - 2) >> 2;       // column half of the 256-wide tile
+        const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+        uint32_t chunk_iter = 0;
+        bool ok = true;
+        for (int64_t t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+            const int64_t mt = t % n_mt, nt = t / n_mt;
+            int32_t acc[128];
+#pragma unroll
+            for (int i = 0; i < 128; ++i) acc[i] = 0;
+            for (int c = 0; c < n_chunks; ++c, ++chunk_iter) {
+                const uint32_t buf = chunk_iter & 1u;
+                if (*abort_flag || !mbar_wait(accf_bar(buf), (chunk_iter >> 1) & 1u)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t taddr = tmem_base + lane_off + buf * BN + h * 128;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    uint32_t r[32];
+                    tmem_ld32(taddr + j * 32, r);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) acc[j * 32 + i] += __float2int_rn(__uint_as_float(r[i]));
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(acce_bar(buf));
+            }
+            if (!ok) break;
+            const int64_t row = mt * BM + q * 32 + lane;
+            if (row >= p.m) continue;
+            const int64_t col0 = nt * BN + h * 128;
+            if constexpr (kRawInt32) {
+                int32_t *dst = p.a + row * p.ldy + col0;
+#pragma unroll
+                for (int j = 0; j < 128; j += 4) {
+                    if (col0 + j + 3 < p.n) {
+                        *reinterpret_cast<int4 *>(dst + j) = make_int4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            if (col0 + j + e < p.n) dst[j + e] = acc[j + e];
+                    }
+                }
+            } else {
+                const float sxr = p.sx[row];
+                float *dst = p.y + row * p.ldy + col0;
+#pragma unroll
+                for (int j = 0; j < 128; j += 4) {
+                    float v[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int64_t col = col0 + j + e;
+                        const int64_t cc = col < p.n ? col : p.n - 1;
+                        const float b = p.bias ? __ldg(p.bias + cc) : 0.0f;
+                        v[e] = fmaf(static_cast<float>(acc[j + e]) * sxr, __ldg(p.sw + cc), b);
+                    }
+                    if (col0 + j + 3 < p.n) {
+                        __stcs(reinterpret_cast<float4 *>(dst + j), make_float4(v[0], v[1], v[2], v[3]));
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            if (col0 + j + e < p.n) dst[j + e] = v[e];
+                    }
+                }
+            }
+        }
+        if (!ok) fail();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
+                     : "memory");
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+// 2-D map over a [rows, ld] bf16 matrix, box = box_rows x 64 elements, 128-byte swizzle.
+bool make_map(CUtensorMap *map, const void *base, int64_t rows, int64_t kpad, int64_t ld, uint32_t box_rows)
+{
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(kpad), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count()
+{
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return n;
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_tc(const GemmArgs &g, cudaStream_t stream)
+{
+    if (g.m == 0 || g.n == 0) return cudaSuccess;
+    CUtensorMap ta, tb;
+    if (!make_map(&ta, g.qx, g.m, g.kpad, g.ldqx, BM) || !make_map(&tb, g.qw, g.n, g.kpad, g.ldqw, BN))
+        return cudaErrorInvalidValue;
+    TcParams p{};
+    p.m = g.m;
+    p.n = g.n;
+    p.kstages = g.kpad / BK;
+    p.sx = g.sx;
+    p.sw = g.sw;
+    p.bias = g.bias;
+    p.y = g.y;
+    p.a = g.a;
+    p.ldy = g.ldy;
+    p.dev_status = g.dev_status;
+    const int64_t tiles = ((g.m + BM - 1) / BM) * ((g.n + BN - 1) / BN);
+    const int sms = sm_count();
+    if (sms <= 0) return cudaErrorInvalidDevice;
+    const unsigned grid = static_cast<unsigned>(tiles < sms ? tiles : sms);
+    if (g.a) {
+        auto k = gemm_tc_kernel<true>;
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        k<<<grid, THREADS, SMEM_BYTES, stream>>>(ta, tb, p);
+    } else {
+        auto k = gemm_tc_kernel<false>;
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        k<<<grid, THREADS, SMEM_BYTES, stream>>>(ta, tb, p);
+    }
+    return cudaGetLastError();
+}
 
 }  // namespace convrot

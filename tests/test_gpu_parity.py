@@ -22,8 +22,8 @@ from . import parity  # noqa: E402
 
 CODES = [cr.CODES_I8, cr.CODES_BF16]
 CODE_IDS = ["i8", "bf16"]
-GEMM_CODES = [cr.CODES_I8]
-GEMM_IDS = ["i8"]
+GEMM_CODES = [cr.CODES_I8, cr.CODES_BF16]
+GEMM_IDS = ["i8", "bf16"]
 
 
 @pytest.fixture(scope="module", autouse=True)
