@@ -61,6 +61,24 @@ def peaks():
             "source": "fallback"}
 
 
+def measured_traffic(workload: str, codes: str):
+    """DRAM bytes per GEMM launch from the committed ncu summary, if the kernel is unchanged since."""
+    import hashlib
+
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(tpath):
+        return None
+    entry = json.load(open(tpath)).get(f"{workload}/{codes}")
+    if not entry:
+        return None
+    src = os.path.join(ROOT, entry["source"])
+    if not os.path.exists(src):
+        return None
+    if hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] != entry["sha256_16"]:
+        return None
+    return entry["gemm_bytes"]
+
+
 # ---------------------------------------------------------------- clocks
 class ClockSampler:
     FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -301,11 +319,7 @@ def run_ours(args):
     gemm_tops = ops / (gemm_avg * 1e-3) / 1e12
     pack_bytes = wl.m * (4 * wl.k + (1 if codes == cr.CODES_I8 else 2) * wl.k + 4)
     pack_gbs = pack_bytes / (pack_avg * 1e-3) / 1e9
-    traffic = None
-    tpath = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(tpath):
-        tr = json.load(open(tpath)).get(f"{wl.name}/{'i8' if codes == cr.CODES_I8 else 'bf16'}", {})
-        traffic = tr.get("gemm_bytes")
+    traffic = measured_traffic(wl.name, "i8" if codes == cr.CODES_I8 else "bf16")
 
     if rank != 0:
         return

@@ -106,10 +106,12 @@ int64_t convrot_ldq(int64_t k);
  *   k      input features, 1 <= k <= CONVROT_MAX_K.
  *   G      4^m with m >= 1, G | k, G <= CONVROT_MAX_GROUP.
  *   out_w  caller-filled q/scale/ldq/codes; receives rows = n, k, G.
+ *   dev_status  as for convrot_linear.
  * Same kernel as convrot_pack_activations.
  */
 convrot_status convrot_quantize_weights(const float *W, int64_t n, int64_t k, int64_t ldw,
-                                        int32_t G, convrot_packed *out_w, cudaStream_t stream);
+                                        int32_t G, convrot_packed *out_w, int32_t *dev_status,
+                                        cudaStream_t stream);
 
 /*
  * Runtime activation pack ("Runtime activation quantization"): rotate each
@@ -119,9 +121,11 @@ convrot_status convrot_quantize_weights(const float *W, int64_t n, int64_t k, in
  *   m      rows (tokens), m >= 0 (0: nothing is launched).
  *   k, G   as for convrot_quantize_weights.
  *   out_x  caller-filled q/scale/ldq/codes; receives rows = m, k, G.
+ *   dev_status  device int32 or NULL; see convrot_linear.
  */
 convrot_status convrot_pack_activations(const float *X, int64_t m, int64_t k, int64_t ldx,
-                                        int32_t G, convrot_packed *out_x, cudaStream_t stream);
+                                        int32_t G, convrot_packed *out_x, int32_t *dev_status,
+                                        cudaStream_t stream);
 
 /*
  * The linear: A = Q_x Q_w^T in exact integer arithmetic, then

@@ -72,9 +72,9 @@ def load() -> ctypes.CDLL:
         P = ctypes.POINTER(_Packed)
         lib.convrot_ldq.argtypes = [i64]
         lib.convrot_ldq.restype = i64
-        lib.convrot_quantize_weights.argtypes = [vp, i64, i64, i64, i32, P, vp]
+        lib.convrot_quantize_weights.argtypes = [vp, i64, i64, i64, i32, P, vp, vp]
         lib.convrot_quantize_weights.restype = ctypes.c_int
-        lib.convrot_pack_activations.argtypes = [vp, i64, i64, i64, i32, P, vp]
+        lib.convrot_pack_activations.argtypes = [vp, i64, i64, i64, i32, P, vp, vp]
         lib.convrot_pack_activations.restype = ctypes.c_int
         lib.convrot_linear.argtypes = [P, P, vp, vp, i64, vp, vp]
         lib.convrot_linear.restype = ctypes.c_int
@@ -153,27 +153,31 @@ def _padded_out(m: int, n: int, dtype, device) -> torch.Tensor:
     return torch.empty((m, ld), dtype=dtype, device=device)[:, :n]
 
 
-def _pack(fn, X: torch.Tensor, G: int, codes: int, out: Packed | None, stream, what: str) -> Packed:
+def _pack(fn, X: torch.Tensor, G: int, codes: int, out: Packed | None, dev_status, stream,
+          what: str) -> Packed:
     if X.dtype != torch.float32 or not X.is_cuda or X.dim() != 2 or X.stride(1) != 1:
         raise TypeError("X must be a 2-D row-major float32 CUDA tensor")
     rows, k = X.shape
     out = out or empty_packed(rows, k, codes, X.device)
     st = out.struct()
-    _check(fn(_ptr(X), rows, k, X.stride(0), int(G), ctypes.byref(st), _stream(stream)), what)
+    _check(fn(_ptr(X), rows, k, X.stride(0), int(G), ctypes.byref(st), _ptr(dev_status), _stream(stream)),
+           what)
     out.rows, out.k, out.group_size = int(st.rows), int(st.k), int(st.group_size)
     return out
 
 
 def convrot_quantize_weights(W: torch.Tensor, G: int, codes: int = CODES_I8, out: Packed | None = None,
-                             stream=None) -> Packed:
+                             dev_status: torch.Tensor | None = None, stream=None) -> Packed:
     """Offline: Q_w, s_w of W [n, k] fp32 (page section "Weight quantization")."""
-    return _pack(load().convrot_quantize_weights, W, G, codes, out, stream, "convrot_quantize_weights")
+    return _pack(load().convrot_quantize_weights, W, G, codes, out, dev_status, stream,
+                 "convrot_quantize_weights")
 
 
 def convrot_pack_activations(X: torch.Tensor, G: int, codes: int = CODES_I8, out: Packed | None = None,
-                             stream=None) -> Packed:
+                             dev_status: torch.Tensor | None = None, stream=None) -> Packed:
     """Runtime: Q_x, s_x of X [m, k] fp32 (page section "Runtime activation quantization")."""
-    return _pack(load().convrot_pack_activations, X, G, codes, out, stream, "convrot_pack_activations")
+    return _pack(load().convrot_pack_activations, X, G, codes, out, dev_status, stream,
+                 "convrot_pack_activations")
 
 
 def convrot_linear(x: Packed, w: Packed, bias: torch.Tensor | None = None, out: torch.Tensor | None = None,

@@ -47,7 +47,7 @@ convrot_status check_packed_buffers(const convrot_packed *p, int64_t rows, int64
 }
 
 convrot_status pack_rows(const float *X, int64_t rows, int64_t k, int64_t ld, int32_t G,
-                         convrot_packed *out, cudaStream_t stream)
+                         convrot_packed *out, int32_t *dev_status, cudaStream_t stream)
 {
     int log4g = 0;
     if (rows < 0 || !out) return CONVROT_ERR_INVALID_ARG;
@@ -59,6 +59,7 @@ convrot_status pack_rows(const float *X, int64_t rows, int64_t k, int64_t ld, in
     if (rows > 0) {
         if (!X) return CONVROT_ERR_INVALID_ARG;
         if (!aligned(X, 16) || ld % 4 != 0) return CONVROT_ERR_ALIGNMENT;
+        if (dev_status && !aligned(dev_status, 4)) return CONVROT_ERR_ALIGNMENT;
     }
     out->rows = rows;
     out->k = k;
@@ -75,6 +76,7 @@ convrot_status pack_rows(const float *X, int64_t rows, int64_t k, int64_t ld, in
     a.kpad = static_cast<int32_t>(convrot_ldq(k));
     a.scale = out->scale;
     a.bf16 = out->codes == CONVROT_CODES_BF16;
+    a.dev_status = dev_status;
     return convrot::launch_pack(a, stream) == cudaSuccess ? CONVROT_OK : CONVROT_ERR_CUDA;
 }
 
@@ -138,15 +140,15 @@ extern "C" {
 int64_t convrot_ldq(int64_t k) { return k <= 0 ? 0 : ((k + 127) / 128) * 128; }
 
 convrot_status convrot_quantize_weights(const float *W, int64_t n, int64_t k, int64_t ldw, int32_t G,
-                                        convrot_packed *out_w, cudaStream_t stream)
+                                        convrot_packed *out_w, int32_t *dev_status, cudaStream_t stream)
 {
-    return pack_rows(W, n, k, ldw, G, out_w, stream);
+    return pack_rows(W, n, k, ldw, G, out_w, dev_status, stream);
 }
 
 convrot_status convrot_pack_activations(const float *X, int64_t m, int64_t k, int64_t ldx, int32_t G,
-                                        convrot_packed *out_x, cudaStream_t stream)
+                                        convrot_packed *out_x, int32_t *dev_status, cudaStream_t stream)
 {
-    return pack_rows(X, m, k, ldx, G, out_x, stream);
+    return pack_rows(X, m, k, ldx, G, out_x, dev_status, stream);
 }
 
 convrot_status convrot_linear(const convrot_packed *x, const convrot_packed *w, const float *bias,

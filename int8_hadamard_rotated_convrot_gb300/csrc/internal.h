@@ -19,6 +19,7 @@ struct PackArgs {
     int32_t kpad;     // columns [k, kpad) of q are written as zero
     float *scale;     // [rows]
     int32_t bf16;     // 0: int8 codes, 1: bf16 codes
+    int32_t *dev_status;  // receives CONVROT_ERR_TIMEOUT if a bounded wait runs out (may be null)
 };
 
 cudaError_t launch_pack(const PackArgs &a, cudaStream_t stream);

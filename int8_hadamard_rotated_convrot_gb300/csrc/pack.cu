@@ -5,98 +5,113 @@
 // "Runtime activation quantization" (the offline "Weight quantization" uses
 // the same formulas on the rows of W):
 //
-//   X_rot = X R        R = normalized Kronecker power of H4 per group of G
+//   X_rot = X R        R = normalized Kronecker power of H4 per group of G = 4^n
 //   s     = max |X_rot| / 127 over the whole row
 //   Q     = clamp(round_half_away(X_rot / s), -127, 127)
 //
 // HBM-bound: X is read once (4 B/element) and the codes written once (1 or
-// 2 B/element). One CTA, or one thread-block cluster for rows longer than a
-// CTA holds, owns a row, keeps it in registers, and never stages it through
-// memory.
+// 2 B/element).
 //
-// Register layout. The row is split into chunks of 32 lanes x S slots x 4
-// floats (128*S floats). Lane l, slot j of a warp holds the float4 with quad
-// index q = chunk*32*S + j*32 + l, so every warp-wide load or store touches
-// consecutive addresses (512 B per instruction for fp32). The element index
-// inside a group, e = 4q + c (c = float4 component), has base-4 digits
-//   d0 = c, d1 = lane bits 0-1, d2 = lane bits 2-3,
-//   d3 = (lane bit 4, slot bit 0), d4 = slot bits 1-2, d5 = slot bits 3-4,
-// so a group of G = 4^n never spans more than one warp: S = 1 for G <= 64,
-// 2 for G = 256, 8 for G = 1024, 32 for G = 4096 (then 128 floats a thread).
+// How R_G is applied. The printed H4 is (1/2) D1 P W1 D1 with W1 = [[1,1],
+// [1,-1]] (x) [[1,1],[1,-1]], D1 = diag(1,1,1,-1) and P the swap of entries 1
+// and 2 (e.g. row 1 of W1 D1 is (1,-1,1,1), which is row 2 of 2*H4). By the
+// mixed-product property of the Kronecker product,
+//   R_G = H4^(x)n = 2^-n * D * Pi * W * D
+// where W is the Walsh-Hadamard matrix of size G (radix-2 butterflies over all
+// 2n index bits), D = diag((-1)^(number of base-4 digits of the index equal
+// to 3)) and Pi swaps the two bits inside every base-4 digit of the index. So
+// the kernel flips input signs by D, runs plain Walsh-Hadamard butterflies
+// (adds and subtracts only), applies D again at the output (folded into the
+// quantization multiplier; D is invariant under Pi) and writes each value to
+// its Pi-permuted position. The factor 2^-n is exact and folded into the scale.
 //
-// One radix-4 stage along a digit replaces every 4-tuple (x_0..x_3) that
-// differs only in that digit by H4 x, i.e. (H4 rows are the printed matrix
-// / 2, a minus sign where row + column = 3)
-//   y_D = ((x_D + x_{D^1}) + (x_{D^2} - x_{D^3})) / 2.
-// Applying it along every digit of the in-group index is R_G applied to the
-// group, by the mixed-product property of the Kronecker product. Partners in
-// another lane come from warp shuffles, partners in another slot or
-// component are registers.
+// Register layout. A thread holds S float4 "slots". In a tile of 2^LANES
+// consecutive threads, thread l, slot j holds the float4 with quad index
+//   q = tile * S * 2^LANES + j * 2^LANES + l,
+// so a warp-wide access of one slot touches 2^LANES consecutive quads per
+// tile. The in-group quad index is q mod G/4; its low bits come from the lane
+// (butterflies by warp shuffle) and the rest from the slot (register
+// butterflies). The float4 component is digit 0 of the in-group index.
+//
+// Two kernels share this arithmetic:
+//   pack_ring_kernel  persistent, one CTA per SM; whole rows stream into a
+//                     shared-memory ring by bulk copies (cp.async.bulk) with
+//                     mbarrier completion, several stages ahead of the math.
+//   pack_direct_kernel rows too long for the ring: registers are loaded from
+//                     global memory directly and a thread-block cluster may
+//                     own one row (absmax exchanged through distributed
+//                     shared memory).
 #include <cuda_bf16.h>
 
+#include "../../include/convrot.h"
 #include "internal.h"
 
 namespace convrot {
 namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
+constexpr uint32_t kSign = 0x80000000u;
+constexpr int kMaxStages = 4;
+constexpr uint64_t kTimeoutNs = 4000000000ull;  // 4 s
 
-// y_D = ((x_D + x_{D^1}) + (x_{D^2} - x_{D^3})) / 2 given the three partners.
-__device__ __forceinline__ float h4_out(float x, float p1, float p2, float p3)
+template <int S>
+constexpr int kMaxThreads = S >= 32 ? 256 : 512;
+
+// Pi on an in-group quad index of `bits` bits: swap the two bits of every
+// base-4 digit (quad-index bit pairs (0,1), (2,3), ...).
+__device__ __forceinline__ uint32_t swap_digit_bits(uint32_t g, int bits)
 {
-    return 0.5f * ((x + p1) + (p2 - p3));
+    const uint32_t mask = (1u << bits) - 1u;
+    return (((g & 0x55555555u) << 1) | ((g >> 1) & 0x55555555u)) & mask;
 }
 
-__device__ __forceinline__ void h4_inplace(float &a, float &b, float &c, float &d)
+// Sign of D from the in-group quad index (digits 1..n-1; digit 0 is the component).
+__device__ __forceinline__ uint32_t quad_sign(uint32_t g)
 {
-    const float ya = h4_out(a, b, c, d);
-    const float yb = h4_out(b, a, d, c);
-    const float yc = h4_out(c, d, a, b);
-    const float yd = h4_out(d, c, b, a);
-    a = ya;
-    b = yb;
-    c = yc;
-    d = yd;
+    return (__popc(g & (g >> 1) & 0x55555555u) & 1) ? kSign : 0u;
 }
 
-// Digit held by two lane bits (masks m1 = low bit, m2 = high bit).
-__device__ __forceinline__ float lane_digit(float x, int m1, int m2)
+__device__ __forceinline__ float xor_sign(float x, uint32_t m) { return __uint_as_float(__float_as_uint(x) ^ m); }
+
+// Round half away from zero. For a >= 0, floor(a + 1/2) is the answer; the sum
+// rounded toward zero has the same floor (it never drops below an integer the
+// exact sum reaches), and it cannot round up across an integer the way a
+// round-to-nearest sum can just below 1/2.
+__device__ __forceinline__ float round_half_away(float v)
 {
-    const float p1 = __shfl_xor_sync(kFull, x, m1);
-    const float p2 = __shfl_xor_sync(kFull, x, m2);
-    const float p3 = __shfl_xor_sync(kFull, x, m1 | m2);
-    return h4_out(x, p1, p2, p3);
+    return copysignf(truncf(__fadd_rz(fabsf(v), 0.5f)), v);
 }
 
-__device__ __forceinline__ float4 lane_digit4(float4 v, int m1, int m2)
+__device__ __forceinline__ uint64_t globaltimer()
 {
-    return make_float4(lane_digit(v.x, m1, m2), lane_digit(v.y, m1, m2),
-                       lane_digit(v.z, m1, m2), lane_digit(v.w, m1, m2));
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
 }
 
-__device__ __forceinline__ float4 f4_h4(float4 x, float4 p1, float4 p2, float4 p3)
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 {
-    return make_float4(h4_out(x.x, p1.x, p2.x, p3.x), h4_out(x.y, p1.y, p2.y, p3.y),
-                       h4_out(x.z, p1.z, p2.z, p3.z), h4_out(x.w, p1.w, p2.w, p3.w));
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
 }
 
-__device__ __forceinline__ float4 shfl_xor4(float4 v, int m)
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
 {
-    return make_float4(__shfl_xor_sync(kFull, v.x, m), __shfl_xor_sync(kFull, v.y, m),
-                       __shfl_xor_sync(kFull, v.z, m), __shfl_xor_sync(kFull, v.w, m));
-}
-
-__device__ __forceinline__ float absmax4(float m, float4 v)
-{
-    return fmaxf(m, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
-}
-
-// Round half away from zero, clamp to [-127, 127].
-__device__ __forceinline__ int code_of(float x, float s)
-{
-    float v = roundf(__fdiv_rn(x, s));
-    v = fminf(fmaxf(v, -127.0f), 127.0f);
-    return static_cast<int>(v);
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    for (;;) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer() - t0 > kTimeoutNs) return false;
+    }
 }
 
 __device__ __forceinline__ uint32_t cluster_smem_addr(const void *p, uint32_t rank)
@@ -120,241 +135,440 @@ __device__ __forceinline__ void cluster_sync_all()
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// 128 floats a thread (S = 32) need up to 255 registers: at most 8 warps.
-template <int S>
-constexpr int kPackMaxThreads = S == 32 ? 256 : 1024;
+// Where one thread's slots sit along a row.
+template <int LANES, int S>
+struct Place {
+    int l_in;        // lane inside the tile
+    int64_t q0;      // quad index of slot 0
+    int lbg, sbg;    // lane / slot bits inside a group
+    uint32_t gmask;  // in-group quad-index mask
+    int qbits;
 
-template <int S, int CPT, bool kBf16>
-__global__ void __launch_bounds__(kPackMaxThreads<S>) pack_kernel(PackArgs a, int cl, int64_t row0)
+    __device__ __forceinline__ Place(int t_row, int n)
+    {
+        l_in = t_row & ((1 << LANES) - 1);
+        q0 = static_cast<int64_t>(t_row >> LANES) * (S << LANES) + l_in;
+        qbits = 2 * n - 2;
+        lbg = qbits < LANES ? qbits : LANES;
+        sbg = qbits - lbg;
+        gmask = (1u << qbits) - 1u;
+    }
+    __device__ __forceinline__ int64_t quad(int j) const { return q0 + static_cast<int64_t>(j) * (1 << LANES); }
+    __device__ __forceinline__ uint32_t group_index(int j) const { return static_cast<uint32_t>(quad(j)) & gmask; }
+};
+
+// D, then the Walsh-Hadamard butterflies over all 2n in-group bits.
+template <int LANES, int S>
+__device__ __forceinline__ void rotate(float4 (&v)[S], const Place<LANES, S> &pl)
 {
-    const int lane = threadIdx.x & 31;
-    const int warp = threadIdx.x >> 5;
-    const int nw = blockDim.x >> 5;
-    const int64_t row = row0 + blockIdx.x / cl;
-    const int cr = blockIdx.x % cl;  // rank inside the cluster (cluster dims are (cl,1,1))
-
-    const int chunk_quads = 32 * S;
-    const int n_chunks = a.kpad / (4 * chunk_quads);  // kpad is a multiple of 128*S
-    const int per_cta = (n_chunks + cl - 1) / cl;
-    const int kq = a.k >> 2;           // quads that hold data
-    const int kpq = a.kpad >> 2;       // quads written (data + zero pad)
-
-    const float4 *xrow = reinterpret_cast<const float4 *>(a.x + row * a.ldx);
-    float4 v[CPT][S];
-    int chunk[CPT];
-
 #pragma unroll
-    for (int t = 0; t < CPT; ++t) {
-        const int local = warp + nw * t;
-        chunk[t] = (local < per_cta) ? cr * per_cta + local : n_chunks;
+    for (int j = 0; j < S; ++j) {
+        const uint32_t sg = quad_sign(pl.group_index(j));
+        v[j].x = xor_sign(v[j].x, sg);
+        v[j].y = xor_sign(v[j].y, sg);
+        v[j].z = xor_sign(v[j].z, sg);
+        v[j].w = xor_sign(v[j].w, sg ^ kSign);  // component 3: digit 0 equal to 3
+        const float s0 = v[j].x + v[j].y, d0 = v[j].x - v[j].y;
+        const float s1 = v[j].z + v[j].w, d1 = v[j].z - v[j].w;
+        v[j] = make_float4(s0 + s1, d0 + d1, s0 - s1, d0 - d1);
+    }
+#pragma unroll
+    for (int b = 0; b < LANES; ++b) {
+        if (b >= pl.lbg) break;
+        const float sg = ((pl.l_in >> b) & 1) ? -1.0f : 1.0f;
 #pragma unroll
         for (int j = 0; j < S; ++j) {
-            const int q = chunk[t] * chunk_quads + j * 32 + lane;
-            v[t][j] = (chunk[t] < n_chunks && q < kq) ? __ldcs(xrow + q)
-                                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+            v[j].x = fmaf(sg, v[j].x, __shfl_xor_sync(kFull, v[j].x, 1 << b));
+            v[j].y = fmaf(sg, v[j].y, __shfl_xor_sync(kFull, v[j].y, 1 << b));
+            v[j].z = fmaf(sg, v[j].z, __shfl_xor_sync(kFull, v[j].z, 1 << b));
+            v[j].w = fmaf(sg, v[j].w, __shfl_xor_sync(kFull, v[j].w, 1 << b));
         }
     }
+#pragma unroll
+    for (int b = 0; (1 << b) < S; ++b) {
+        if (b >= pl.sbg) break;
+#pragma unroll
+        for (int j = 0; j < S; ++j) {
+            if (j & (1 << b)) continue;
+            const int k = j | (1 << b);
+            const float4 x = v[j], y = v[k];
+            v[j] = make_float4(x.x + y.x, x.y + y.y, x.z + y.z, x.w + y.w);
+            v[k] = make_float4(x.x - y.x, x.y - y.y, x.z - y.z, x.w - y.w);
+        }
+    }
+}
 
-    const int n = a.log4g;
-    // digit 0: the float4 components
-#pragma unroll
-    for (int t = 0; t < CPT; ++t)
-#pragma unroll
-        for (int j = 0; j < S; ++j) h4_inplace(v[t][j].x, v[t][j].y, v[t][j].z, v[t][j].w);
-    // digits 1 and 2: lane bits 0-1 and 2-3
-    if (n > 1) {
-#pragma unroll
-        for (int t = 0; t < CPT; ++t)
-#pragma unroll
-            for (int j = 0; j < S; ++j) v[t][j] = lane_digit4(v[t][j], 1, 2);
-    }
-    if (n > 2) {
-#pragma unroll
-        for (int t = 0; t < CPT; ++t)
-#pragma unroll
-            for (int j = 0; j < S; ++j) v[t][j] = lane_digit4(v[t][j], 4, 8);
-    }
-    // digit 3: lane bit 4 (low) and slot bit 0 (high)
-    if constexpr (S >= 2) {
-        if (n > 3) {
-#pragma unroll
-            for (int t = 0; t < CPT; ++t) {
-                float4 sh[S];
-#pragma unroll
-                for (int j = 0; j < S; ++j) sh[j] = shfl_xor4(v[t][j], 16);
-                float4 nv[S];
-#pragma unroll
-                for (int j = 0; j < S; ++j) nv[j] = f4_h4(v[t][j], sh[j], v[t][j ^ 1], sh[j ^ 1]);
-#pragma unroll
-                for (int j = 0; j < S; ++j) v[t][j] = nv[j];
-            }
-        }
-    }
-    // digit 4: slot bits 1-2
-    if constexpr (S >= 8) {
-        if (n > 4) {
-#pragma unroll
-            for (int t = 0; t < CPT; ++t) {
-                float4 nv[S];
-#pragma unroll
-                for (int j = 0; j < S; ++j)
-                    nv[j] = f4_h4(v[t][j], v[t][j ^ 2], v[t][j ^ 4], v[t][j ^ 6]);
-#pragma unroll
-                for (int j = 0; j < S; ++j) v[t][j] = nv[j];
-            }
-        }
-    }
-    // digit 5: slot bits 3-4
-    if constexpr (S >= 32) {
-        if (n > 5) {
-#pragma unroll
-            for (int t = 0; t < CPT; ++t) {
-                float4 nv[S];
-#pragma unroll
-                for (int j = 0; j < S; ++j)
-                    nv[j] = f4_h4(v[t][j], v[t][j ^ 8], v[t][j ^ 16], v[t][j ^ 24]);
-#pragma unroll
-                for (int j = 0; j < S; ++j) v[t][j] = nv[j];
-            }
-        }
-    }
-
-    // absmax over the whole rotated row (padding lanes hold zeros)
+template <int S>
+__device__ __forceinline__ float absmax(const float4 (&v)[S])
+{
     float m = 0.0f;
 #pragma unroll
-    for (int t = 0; t < CPT; ++t)
-#pragma unroll
-        for (int j = 0; j < S; ++j) m = absmax4(m, v[t][j]);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, off));
+    for (int j = 0; j < S; ++j)
+        m = fmaxf(m, fmaxf(fmaxf(fabsf(v[j].x), fabsf(v[j].y)), fmaxf(fabsf(v[j].z), fabsf(v[j].w))));
+    return m;
+}
 
-    __shared__ float warp_max[32];
-    __shared__ float cta_max;
-    if (lane == 0) warp_max[warp] = m;
-    __syncthreads();
-    if (warp == 0) {
-        float mm = (lane < nw) ? warp_max[lane] : 0.0f;
+// Codes of one thread's slots, written to their Pi-permuted places (D folded into inv).
+template <int LANES, int S, bool kBf16>
+__device__ __forceinline__ void quantize_store(const float4 (&v)[S], const Place<LANES, S> &pl, char *qrow, int kq,
+                                               float inv)
+{
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) mm = fmaxf(mm, __shfl_xor_sync(kFull, mm, off));
-        if (lane == 0) cta_max = mm;
+    for (int j = 0; j < S; ++j) {
+        const int64_t q = pl.quad(j);
+        if (q >= kq) continue;
+        const uint32_t g = pl.group_index(j);
+        const int64_t q_out = q - g + swap_digit_bits(g, pl.qbits);
+        const float ip = xor_sign(inv, quad_sign(g)), in = xor_sign(ip, kSign);
+        // Pi on digit 0: components 1 and 2 trade places
+        const float r0 = round_half_away(v[j].x * ip);
+        const float r1 = round_half_away(v[j].z * ip);
+        const float r2 = round_half_away(v[j].y * ip);
+        const float r3 = round_half_away(v[j].w * in);
+        if constexpr (kBf16) {
+            // |r| <= 127: the bf16 of r is the top half of its fp32 bits (+0 turns -0 into 0)
+            const uint32_t lo = __byte_perm(__float_as_uint(r0 + 0.0f), __float_as_uint(r1 + 0.0f), 0x7632);
+            const uint32_t hi = __byte_perm(__float_as_uint(r2 + 0.0f), __float_as_uint(r3 + 0.0f), 0x7632);
+            reinterpret_cast<uint2 *>(qrow)[q_out] = make_uint2(lo, hi);
+        } else {
+            // r + 1.5 * 2^23 holds r in its low mantissa bits: the low byte is r as int8
+            constexpr float kMagic = 12582912.0f;
+            const uint32_t w0 = __float_as_uint(r0 + kMagic), w1 = __float_as_uint(r1 + kMagic);
+            const uint32_t w2 = __float_as_uint(r2 + kMagic), w3 = __float_as_uint(r3 + kMagic);
+            reinterpret_cast<uint32_t *>(qrow)[q_out] =
+                __byte_perm(__byte_perm(w0, w1, 0x0040), __byte_perm(w2, w3, 0x0040), 0x5410);
+        }
+    }
+}
+
+template <bool kBf16>
+__device__ __forceinline__ void zero_pad(char *qrow, int kq, int kpq, int t_row, int row_threads)
+{
+    for (int i = kq + t_row; i < kpq; i += row_threads) {
+        if constexpr (kBf16)
+            reinterpret_cast<uint2 *>(qrow)[i] = make_uint2(0u, 0u);
+        else
+            reinterpret_cast<uint32_t *>(qrow)[i] = 0u;
+    }
+}
+
+// Scale s = max|X_rot| / 127 and the multiplier 2^-n / s applied to the
+// unnormalized butterfly output (0 for an all-zero row).
+__device__ __forceinline__ float scale_of(float amax_unnorm, int n, float *inv)
+{
+    const float s = ldexpf(amax_unnorm, -n) / 127.0f;
+    *inv = s > 0.0f ? ldexpf(__frcp_rn(s), -n) : 0.0f;
+    return s;
+}
+
+struct RingPlan {
+    int threads_per_row;  // multiple of 2^LANES; rows_per_stage * threads_per_row = blockDim.x
+    int rows_per_stage;
+    int stages;
+    uint32_t row_bytes;    // k * 4
+    uint32_t stage_bytes;  // rows_per_stage * row_bytes, rounded up to 128
+};
+
+template <int LANES, int S, bool kBf16>
+__global__ void __launch_bounds__(kMaxThreads<S>) pack_ring_kernel(PackArgs a, RingPlan P)
+{
+    extern __shared__ __align__(128) uint8_t ring[];
+    __shared__ __align__(8) uint64_t full_bar[kMaxStages];
+    __shared__ float part[2][kMaxThreads<S>];
+
+    const int lane = threadIdx.x & 31;
+    const int tpr = P.threads_per_row, R = P.rows_per_stage, NS = P.stages;
+    const int r_local = threadIdx.x / tpr;
+    const int t_row = threadIdx.x - r_local * tpr;
+    const int n = a.log4g;
+    const int kq = a.k >> 2, kpq = a.kpad >> 2;
+    const Place<LANES, S> pl(t_row, n);
+    const int64_t nblocks = (a.rows + R - 1) / R;
+    const uint32_t ring_base = static_cast<uint32_t>(__cvta_generic_to_shared(ring));
+    const uint32_t bar_base = static_cast<uint32_t>(__cvta_generic_to_shared(full_bar));
+    const int seg = (tpr & 31) == 0 ? 32 : (tpr & -tpr);  // power of two dividing tpr, <= 32
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NS; ++s)
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar_base + 8u * s) : "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
-    float amax = cta_max;
-    if (cl > 1) {
-        cluster_sync_all();  // every CTA's cta_max is written
-        for (int r = 0; r < cl; ++r) amax = fmaxf(amax, ld_cluster_f32(cluster_smem_addr(&cta_max, r)));
-    }
 
-    const float s = amax / 127.0f;
-    const bool zero_row = !(s > 0.0f);
-    if (cr == 0 && threadIdx.x == 0) a.scale[row] = s;
+    // one bulk copy per row of the block into the stage; completion counted in bytes on its mbarrier
+    auto issue = [&](int stage, int64_t blk) {
+        if (blk >= nblocks) return;
+        const int64_t r0 = blk * R;
+        const int nr = a.rows - r0 < R ? static_cast<int>(a.rows - r0) : R;
+        const uint32_t bar = bar_base + 8u * stage;
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+                     "r"(static_cast<uint32_t>(nr) * P.row_bytes)
+                     : "memory");
+        for (int i = 0; i < nr; ++i) {
+            const float *src = a.x + (r0 + i) * a.ldx;
+            asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                             ring_base + stage * P.stage_bytes + i * P.row_bytes),
+                         "l"(src), "r"(P.row_bytes), "r"(bar)
+                         : "memory");
+        }
+    };
 
-#pragma unroll
-    for (int t = 0; t < CPT; ++t) {
-        if (chunk[t] >= n_chunks) continue;
+    if (threadIdx.x == 0)
+        for (int s = 0; s < NS - 1; ++s) issue(s, blockIdx.x + static_cast<int64_t>(s) * gridDim.x);
+
+    int it = 0;
+    bool ok = true;
+    for (int64_t blk = blockIdx.x; blk < nblocks; blk += gridDim.x, ++it) {
+        const int stage = it % NS;
+        if (threadIdx.x == 0) {
+            // the stage refilled here was read into registers before the previous barrier
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            issue((it + NS - 1) % NS, blk + static_cast<int64_t>(NS - 1) * gridDim.x);
+        }
+        const bool got = mbar_wait(bar_base + 8u * stage, static_cast<uint32_t>(it / NS) & 1u);
+
+        const int64_t row = blk * R + r_local;
+        const bool row_ok = got && row < a.rows;
+        const float4 *src = reinterpret_cast<const float4 *>(ring + stage * P.stage_bytes + r_local * P.row_bytes);
+        float4 v[S];
 #pragma unroll
         for (int j = 0; j < S; ++j) {
-            const int q = chunk[t] * chunk_quads + j * 32 + lane;
-            if (q >= kpq) continue;
-            int c0 = 0, c1 = 0, c2 = 0, c3 = 0;
-            if (!zero_row && q < kq) {
-                c0 = code_of(v[t][j].x, s);
-                c1 = code_of(v[t][j].y, s);
-                c2 = code_of(v[t][j].z, s);
-                c3 = code_of(v[t][j].w, s);
-            }
-            if constexpr (kBf16) {
-                __nv_bfloat162 lo = __floats2bfloat162_rn(static_cast<float>(c0), static_cast<float>(c1));
-                __nv_bfloat162 hi = __floats2bfloat162_rn(static_cast<float>(c2), static_cast<float>(c3));
-                uint2 packed;
-                packed.x = *reinterpret_cast<uint32_t *>(&lo);
-                packed.y = *reinterpret_cast<uint32_t *>(&hi);
-                reinterpret_cast<uint2 *>(static_cast<__nv_bfloat16 *>(a.q) + row * a.ldq)[q] = packed;
-            } else {
-                const uint32_t packed = (static_cast<uint32_t>(c0) & 0xffu) |
-                                        ((static_cast<uint32_t>(c1) & 0xffu) << 8) |
-                                        ((static_cast<uint32_t>(c2) & 0xffu) << 16) |
-                                        (static_cast<uint32_t>(c3) << 24);
-                reinterpret_cast<uint32_t *>(static_cast<int8_t *>(a.q) + row * a.ldq)[q] = packed;
-            }
+            const int64_t q = pl.quad(j);
+            v[j] = (row_ok && q < kq) ? src[q] : make_float4(0.f, 0.f, 0.f, 0.f);
         }
+        rotate<LANES, S>(v, pl);
+
+        float m = absmax<S>(v);
+        for (int off = seg >> 1; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, off));
+        float *pp = part[it & 1];
+        if ((lane & (seg - 1)) == 0) pp[threadIdx.x / seg] = m;
+        // all threads agree on whether the stage arrived; a failed wait ends the loop everywhere
+        if (!__syncthreads_and(got)) {
+            ok = false;
+            break;
+        }
+        float amax = 0.0f;
+        const int p0 = (r_local * tpr) / seg, np = tpr / seg;
+        for (int i = 0; i < np; ++i) amax = fmaxf(amax, pp[p0 + i]);
+        float inv;
+        const float s = scale_of(amax, n, &inv);
+        if (row < a.rows) {
+            if (t_row == 0) a.scale[row] = s;
+            char *qrow = static_cast<char *>(a.q) + row * a.ldq * (kBf16 ? 2 : 1);
+            quantize_store<LANES, S, kBf16>(v, pl, qrow, kq, inv);
+            zero_pad<kBf16>(qrow, kq, kpq, t_row, tpr);
+        }
+    }
+    if (!ok && threadIdx.x == 0) {
+        if (a.dev_status) atomicExch(a.dev_status, static_cast<int32_t>(CONVROT_ERR_TIMEOUT));
+        // let the copies already issued land before the CTA's shared memory goes away
+        int64_t blk = blockIdx.x + static_cast<int64_t>(it) * gridDim.x;
+        for (int s = 0; s < NS; ++s, blk += gridDim.x)
+            if (blk < nblocks) mbar_wait(bar_base + 8u * ((it + s) % NS), static_cast<uint32_t>((it + s) / NS) & 1u);
+    }
+}
+
+struct DirectPlan {
+    int threads_per_row;  // per CTA
+    int rows_per_cta;
+    int cl;  // CTAs per row (cluster size); rows_per_cta == 1 when cl > 1
+};
+
+template <int LANES, int S, bool kBf16>
+__global__ void __launch_bounds__(kMaxThreads<S>) pack_direct_kernel(PackArgs a, DirectPlan L, int64_t row0)
+{
+    const int lane = threadIdx.x & 31;
+    const int cl = L.cl;
+    const int cr = cl > 1 ? static_cast<int>(blockIdx.x % cl) : 0;
+    const int64_t cta_block = cl > 1 ? blockIdx.x / cl : blockIdx.x;
+    const int tpr = L.threads_per_row;
+    const int r_local = threadIdx.x / tpr;
+    const int t_cta = threadIdx.x - r_local * tpr;
+    const int64_t row = row0 + cta_block * L.rows_per_cta + r_local;
+    const bool row_ok = row < a.rows;
+    const int t_row = cr * tpr + t_cta;
+    const int n = a.log4g;
+    const int kq = a.k >> 2, kpq = a.kpad >> 2;
+    const Place<LANES, S> pl(t_row, n);
+
+    const float4 *src = reinterpret_cast<const float4 *>(a.x + (row_ok ? row : 0) * a.ldx);
+    float4 v[S];
+#pragma unroll
+    for (int j = 0; j < S; ++j) {
+        const int64_t q = pl.quad(j);
+        v[j] = (row_ok && q < kq) ? __ldcs(src + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    rotate<LANES, S>(v, pl);
+
+    float m = absmax<S>(v);
+    const int seg = (tpr & 31) == 0 ? 32 : (tpr & -tpr);
+    for (int off = seg >> 1; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, off));
+    __shared__ float part[kMaxThreads<S>];
+    __shared__ float cta_max;
+    if ((lane & (seg - 1)) == 0) part[threadIdx.x / seg] = m;
+    __syncthreads();
+    float amax = 0.0f;
+    {
+        const int p0 = (r_local * tpr) / seg, np = tpr / seg;
+        for (int i = 0; i < np; ++i) amax = fmaxf(amax, part[p0 + i]);
+    }
+    if (cl > 1) {
+        if (threadIdx.x == 0) cta_max = amax;
+        cluster_sync_all();  // every CTA's cta_max is written
+        amax = 0.0f;
+        for (int r = 0; r < cl; ++r) amax = fmaxf(amax, ld_cluster_f32(cluster_smem_addr(&cta_max, r)));
+    }
+    float inv;
+    const float s = scale_of(amax, n, &inv);
+    if (row_ok) {
+        if (t_row == 0) a.scale[row] = s;
+        char *qrow = static_cast<char *>(a.q) + row * a.ldq * (kBf16 ? 2 : 1);
+        quantize_store<LANES, S, kBf16>(v, pl, qrow, kq, inv);
+        zero_pad<kBf16>(qrow, kq, kpq, t_row, tpr * cl);
     }
     if (cl > 1) cluster_sync_all();  // no CTA leaves while another may still read its cta_max
 }
 
-struct PackPlan {
-    int S, cpt, warps, cl;
+struct Shape {
+    int lanes, S;
 };
 
-// Chooses slots per chunk S from G, then the smallest cluster and the
-// fewest floats per thread that keep a CTA at <= 16 warps (<= 32 if needed).
-PackPlan plan_pack(int log4g, int kpad)
+Shape shape_for(int log4g)
 {
-    PackPlan p{};
-    p.S = log4g <= 3 ? 1 : (log4g == 4 ? 2 : (log4g == 5 ? 8 : 32));
-    static const int opts1[] = {1, 2, 4, 8}, opts2[] = {1, 2, 4}, opts8[] = {1}, opts32[] = {1};
-    const int *opts = p.S == 1 ? opts1 : (p.S == 2 ? opts2 : (p.S == 8 ? opts8 : opts32));
-    const int n_opts = p.S == 1 ? 4 : (p.S == 2 ? 3 : 1);
-    const int pref_warps = p.S == 32 ? 8 : 16;
-    const int max_warps = p.S == 32 ? 8 : 32;
-    const int n_chunks = kpad / (128 * p.S);
-    for (int limit : {pref_warps, max_warps}) {
-        for (int cl = 1; cl <= 8; ++cl) {
-            const int per_cta = (n_chunks + cl - 1) / cl;
-            for (int i = 0; i < n_opts; ++i) {
-                const int warps = (per_cta + opts[i] - 1) / opts[i];
-                if (warps <= limit) {
-                    p.cpt = opts[i];
-                    p.warps = warps;
-                    p.cl = cl;
-                    return p;
-                }
-            }
-        }
-    }
-    p.cpt = 0;  // no plan (cannot happen for kpad <= 8 CTAs' worth)
-    return p;
+    if (log4g <= 4) return {3, 8};   // G <= 256
+    if (log4g == 5) return {5, 8};   // G = 1024
+    return {5, 32};                  // G = 4096
 }
 
-template <int S, int CPT, bool kBf16>
-cudaError_t launch_one(const PackArgs &a, const PackPlan &p, cudaStream_t stream)
+int gcd_int(int x, int y)
 {
-    const int64_t max_rows = (int64_t{1} << 31) / p.cl - 1;
-    for (int64_t r0 = 0; r0 < a.rows; r0 += max_rows) {
-        const int64_t rows = a.rows - r0 < max_rows ? a.rows - r0 : max_rows;
+    while (y) {
+        const int t = x % y;
+        x = y;
+        y = t;
+    }
+    return x;
+}
+
+int threads_per_row(const Shape &sh, int k)
+{
+    const int tile_q = sh.S << sh.lanes;
+    const int tiles = (k / 4 + tile_q - 1) / tile_q;
+    return tiles << sh.lanes;
+}
+
+constexpr uint32_t kStageTarget = 64 * 1024;
+constexpr uint32_t kRingBytes = 200 * 1024;
+
+// Ring plan, or stages == 0 when rows are too long for it.
+RingPlan ring_plan(const Shape &sh, int k)
+{
+    RingPlan P{};
+    const int T = threads_per_row(sh, k);
+    const int max_threads = sh.S >= 32 ? 256 : 512;
+    const int step = 32 / gcd_int(T, 32);  // rows per stage must fill whole warps
+    P.row_bytes = static_cast<uint32_t>(k) * 4u;
+    if (step * T > max_threads || static_cast<uint64_t>(step) * P.row_bytes > kStageTarget) return P;
+    int R = step;
+    while ((R + step) * T <= max_threads && static_cast<uint64_t>(R + step) * P.row_bytes <= kStageTarget) R += step;
+    P.threads_per_row = T;
+    P.rows_per_stage = R;
+    P.stage_bytes = (R * P.row_bytes + 127u) & ~127u;
+    int ns = static_cast<int>(kRingBytes / P.stage_bytes);
+    P.stages = ns > kMaxStages ? kMaxStages : ns;
+    if (P.stages < 2) P.stages = 0;
+    return P;
+}
+
+DirectPlan direct_plan(const Shape &sh, int k)
+{
+    const int T = threads_per_row(sh, k);
+    const int max_threads = sh.S >= 32 ? 256 : 512;
+    DirectPlan L{};
+    const int step = 32 / gcd_int(T, 32);
+    if (T <= max_threads && step * T <= max_threads) {
+        L.cl = 1;
+        L.threads_per_row = T;
+        int R = step;
+        while (R * T < 256 && (R + step) * T <= max_threads) R += step;
+        L.rows_per_cta = R;
+    } else if (T <= max_threads) {
+        L.cl = 1;
+        L.threads_per_row = (T + 31) / 32 * 32;  // one row per CTA, trailing threads idle
+        L.rows_per_cta = 1;
+    } else {
+        int cl = (T + max_threads - 1) / max_threads;
+        int per = (T + cl - 1) / cl;
+        per = (per + 31) / 32 * 32;  // whole warps, a multiple of 2^LANES (<= 32)
+        cl = (T + per - 1) / per;
+        L.cl = cl;
+        L.threads_per_row = per;
+        L.rows_per_cta = 1;
+    }
+    return L;
+}
+
+int sm_count()
+{
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return n;
+}
+
+template <int LANES, int S, bool kBf16>
+cudaError_t launch_shape(const PackArgs &a, cudaStream_t stream)
+{
+    const Shape sh{LANES, S};
+    const RingPlan P = ring_plan(sh, a.k);
+    if (P.stages > 0) {
+        auto kern = pack_ring_kernel<LANES, S, kBf16>;
+        const int smem = static_cast<int>(P.stages * P.stage_bytes);
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        const int64_t nblocks = (a.rows + P.rows_per_stage - 1) / P.rows_per_stage;
+        const int sms = sm_count();
+        if (sms <= 0) return cudaErrorInvalidDevice;
+        const int64_t grid = nblocks < sms ? nblocks : sms;
+        kern<<<static_cast<unsigned>(grid), P.threads_per_row * P.rows_per_stage, smem, stream>>>(a, P);
+        return cudaGetLastError();
+    }
+    const DirectPlan L = direct_plan(sh, a.k);
+    if (L.cl > 16) return cudaErrorInvalidConfiguration;
+    const int64_t row_blocks = (a.rows + L.rows_per_cta - 1) / L.rows_per_cta;
+    const int64_t max_blocks = (int64_t{1} << 31) / L.cl - 1;
+    for (int64_t b0 = 0; b0 < row_blocks; b0 += max_blocks) {
+        const int64_t blocks = row_blocks - b0 < max_blocks ? row_blocks - b0 : max_blocks;
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(static_cast<unsigned>(rows * p.cl), 1, 1);
-        cfg.blockDim = dim3(static_cast<unsigned>(32 * p.warps), 1, 1);
+        cfg.gridDim = dim3(static_cast<unsigned>(blocks * L.cl), 1, 1);
+        cfg.blockDim = dim3(static_cast<unsigned>(L.threads_per_row * L.rows_per_cta), 1, 1);
         cfg.dynamicSmemBytes = 0;
         cfg.stream = stream;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = static_cast<unsigned>(p.cl);
+        attr[0].val.clusterDim.x = static_cast<unsigned>(L.cl);
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        cudaError_t e = cudaLaunchKernelEx(&cfg, pack_kernel<S, CPT, kBf16>, a, p.cl, r0);
+        auto kern = pack_direct_kernel<LANES, S, kBf16>;
+        if (L.cl > 8) {
+            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+            if (e != cudaSuccess) return e;
+        }
+        cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a, L, b0 * L.rows_per_cta);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
 }
 
 template <bool kBf16>
-cudaError_t dispatch(const PackArgs &a, const PackPlan &p, cudaStream_t stream)
+cudaError_t dispatch(const PackArgs &a, cudaStream_t stream)
 {
-    switch (p.S * 100 + p.cpt) {
-    case 101: return launch_one<1, 1, kBf16>(a, p, stream);
-    case 102: return launch_one<1, 2, kBf16>(a, p, stream);
-    case 104: return launch_one<1, 4, kBf16>(a, p, stream);
-    case 108: return launch_one<1, 8, kBf16>(a, p, stream);
-    case 201: return launch_one<2, 1, kBf16>(a, p, stream);
-    case 202: return launch_one<2, 2, kBf16>(a, p, stream);
-    case 204: return launch_one<2, 4, kBf16>(a, p, stream);
-    case 801: return launch_one<8, 1, kBf16>(a, p, stream);
-    case 3201: return launch_one<32, 1, kBf16>(a, p, stream);
-    default: return cudaErrorInvalidConfiguration;
-    }
+    if (a.log4g <= 4) return launch_shape<3, 8, kBf16>(a, stream);
+    if (a.log4g == 5) return launch_shape<5, 8, kBf16>(a, stream);
+    if (a.log4g == 6) return launch_shape<5, 32, kBf16>(a, stream);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace
@@ -362,9 +576,7 @@ cudaError_t dispatch(const PackArgs &a, const PackPlan &p, cudaStream_t stream)
 cudaError_t launch_pack(const PackArgs &a, cudaStream_t stream)
 {
     if (a.rows == 0) return cudaSuccess;
-    const PackPlan p = plan_pack(a.log4g, a.kpad);
-    if (p.cpt == 0) return cudaErrorInvalidConfiguration;
-    return a.bf16 ? dispatch<true>(a, p, stream) : dispatch<false>(a, p, stream);
+    return a.bf16 ? dispatch<true>(a, stream) : dispatch<false>(a, stream);
 }
 
 }  // namespace convrot

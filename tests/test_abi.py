@@ -63,7 +63,7 @@ def packed(q=FAKE, scale=FAKE, ldq=128, codes=cr.CODES_I8, rows=0, k=0, G=0):
 
 def pack(lib, X=FAKE, m=4, k=256, ldx=256, G=256, out=None):
     out = out or packed(ldq=cr.convrot_ldq(k) if k > 0 else 128)
-    return lib.convrot_pack_activations(X, m, k, ldx, G, ctypes.byref(out), None)
+    return lib.convrot_pack_activations(X, m, k, ldx, G, ctypes.byref(out), None, None)
 
 
 @pytest.mark.parametrize("G", [1, 2, 8, 32, 128, 0, -4, 16384])
@@ -86,7 +86,7 @@ def test_pack_rejects_bad_pointers_and_lds(lib):
     assert pack(lib, ldx=255) == cr.ERR_INVALID_ARG
     assert pack(lib, k=256, ldx=258) == cr.ERR_ALIGNMENT
     assert pack(lib, m=-1) == cr.ERR_INVALID_ARG
-    assert lib.convrot_pack_activations(FAKE, 4, 256, 256, 256, None, None) == cr.ERR_INVALID_ARG
+    assert lib.convrot_pack_activations(FAKE, 4, 256, 256, 256, None, None, None) == cr.ERR_INVALID_ARG
     assert pack(lib, out=packed(q=None)) == cr.ERR_INVALID_ARG
     assert pack(lib, out=packed(scale=None)) == cr.ERR_INVALID_ARG
     assert pack(lib, out=packed(q=FAKE + 8, ldq=256)) == cr.ERR_ALIGNMENT
@@ -97,10 +97,10 @@ def test_pack_rejects_bad_pointers_and_lds(lib):
 
 def test_pack_empty_is_noop_and_fills_shape(lib):
     out = packed(q=None, scale=None, ldq=256)
-    assert lib.convrot_pack_activations(None, 0, 256, 256, 64, ctypes.byref(out), None) == cr.OK
+    assert lib.convrot_pack_activations(None, 0, 256, 256, 64, ctypes.byref(out), None, None) == cr.OK
     assert (out.rows, out.k, out.group_size) == (0, 256, 64)
     out = packed(q=None, scale=None, ldq=256)
-    assert lib.convrot_quantize_weights(None, 0, 192, 192, 64, ctypes.byref(out), None) == cr.OK
+    assert lib.convrot_quantize_weights(None, 0, 192, 192, 64, ctypes.byref(out), None, None) == cr.OK
 
 
 def pair(mx=4, nw=4, k=256, G=256, codes=cr.CODES_I8):
