@@ -41,7 +41,7 @@ namespace convrot {
 namespace {
 
 constexpr int BM = 128, BN = 256, BK = 64;  // BK bf16 = 128 B = one swizzle span
-constexpr int STAGES = 4;
+constexpr int STAGES = 3;
 constexpr int UMMA_K = 16;
 constexpr int CHUNK_KSTAGES = 1024 / BK;  // K elements per exact fp32 chunk / BK
 constexpr int A_BYTES = BM * BK * 2;
@@ -51,7 +51,12 @@ constexpr int EPI_WARPS = 8;
 constexpr int THREADS = 64 + EPI_WARPS * 32;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int BAR_BYTES = 256;
-constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
+// Y staging for TMA stores: per epilogue warp, two 32 x 32 fp32 boxes (4 KB each).
+constexpr int OUT_BOX = 32;
+constexpr int OUT_BUF_BYTES = OUT_BOX * OUT_BOX * 4;
+constexpr int OUT_WARP_BYTES = 2 * OUT_BUF_BYTES;
+constexpr int OUT_BYTES = 8 * OUT_WARP_BYTES;
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + OUT_BYTES + BAR_BYTES;
 constexpr uint64_t kTimeoutNs = 4000000000ull;  // 4 s
 
 // instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major, M = 128, N = 256
@@ -168,23 +173,103 @@ struct TcParams {
     int32_t *dev_status;
 };
 
+
+// One epilogue warp's 32 rows x 128 columns of the tile (lane i holds row
+// row0 + i in acc[]): raw int32 A, or Y = float(A) * s_x[row] * s_w[col] +
+// b[col]. Each 32 x 32 box is written to one of the warp's two shared-memory
+// buffers in the 128-byte-swizzled layout (16-byte chunk c of row r at c ^
+// (r & 7): conflict-free for the row-per-lane writes) and stored by TMA, which
+// writes whole lines and clips rows >= m. A box that would cross column n is
+// written directly with masked stores instead. A buffer is reused only after
+// the store issued from it two boxes earlier has read it.
+template <bool kRawInt32>
+__device__ __forceinline__ void store_tile_rows(const TcParams &p, const CUtensorMap *tmY, uint32_t out_smem,
+                                                uint32_t &store_iter, int64_t row0, int64_t col0,
+                                                const int32_t (&acc)[128], int lane)
+{
+    const int64_t row = row0 + lane;
+    float sxr = 0.0f;
+    if constexpr (!kRawInt32) sxr = row < p.m ? p.sx[row] : 0.0f;
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc) {
+        const int64_t x = col0 + cc * 32;
+        if (x >= p.n) break;
+        if (x + 32 > p.n) {
+            // ragged last box: masked stores straight from registers
+            if (row < p.m) {
+                for (int j = 0; j < 32 && x + j < p.n; ++j) {
+                    const int64_t col = x + j;
+                    if constexpr (kRawInt32) {
+                        p.a[row * p.ldy + col] = acc[cc * 32 + j];
+                    } else {
+                        const float b = p.bias ? __ldg(p.bias + col) : 0.0f;
+                        p.y[row * p.ldy + col] = fmaf(static_cast<float>(acc[cc * 32 + j]) * sxr, __ldg(p.sw + col), b);
+                    }
+                }
+            }
+            continue;
+        }
+        const uint32_t buf = out_smem + (store_iter & 1u) * OUT_BUF_BYTES;
+        if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+        __syncwarp();
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int j = cc * 32 + c * 4 + e;
+                if constexpr (kRawInt32) {
+                    w[e] = static_cast<uint32_t>(acc[j]);
+                } else {
+                    const int64_t col = x + c * 4 + e;
+                    const float b = p.bias ? __ldg(p.bias + col) : 0.0f;
+                    w[e] = __float_as_uint(fmaf(static_cast<float>(acc[j]) * sxr, __ldg(p.sw + col), b));
+                }
+            }
+            const uint32_t addr = buf + lane * (OUT_BOX * 4) + ((c ^ (lane & 7)) << 4);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[0]), "r"(w[1]), "r"(w[2]),
+                         "r"(w[3])
+                         : "memory");
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) {
+            if (row0 < p.m)
+                asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                                 reinterpret_cast<uint64_t>(tmY)),
+                             "r"(static_cast<int>(x)), "r"(static_cast<int>(row0)), "r"(buf)
+                             : "memory");
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        }
+        ++store_iter;
+    }
+}
+
+// The warp's outstanding TMA stores have completed (before the CTA exits).
+__device__ __forceinline__ void drain_stores(int lane)
+{
+    if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+    __syncwarp();
+}
+
 template <bool kRawInt32>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   TcParams p)
+                   const __grid_constant__ CUtensorMap tmY, TcParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = static_cast<uint32_t>(__cvta_generic_to_shared(smem_raw));
     const uint32_t base = (raw + 1023u) & ~1023u;  // swizzle atoms need 1024-byte alignment
     uint8_t *gbase = smem_raw + (base - raw);
-    const uint32_t bars = base + STAGES * STAGE_BYTES;
+    const uint32_t out_base = base + STAGES * STAGE_BYTES;
+    const uint32_t bars = out_base + OUT_BYTES;
     auto full_bar = [&](int s) { return bars + 8u * s; };
     auto empty_bar = [&](int s) { return bars + 8u * (STAGES + s); };
     auto accf_bar = [&](int b) { return bars + 8u * (2 * STAGES + b); };
     auto acce_bar = [&](int b) { return bars + 8u * (2 * STAGES + 2 + b); };
     const uint32_t done_bar = bars + 8u * (2 * STAGES + 4);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + STAGES * STAGE_BYTES + 128);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + STAGES * STAGE_BYTES + 132);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + STAGES * STAGE_BYTES + OUT_BYTES + 128);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + STAGES * STAGE_BYTES + OUT_BYTES + 132);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t n_mt = (p.m + BM - 1) / BM, n_nt = (p.n + BN - 1) / BN;
@@ -206,6 +291,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmY)) : "memory");
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -311,6 +397,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int q = warp & 3;              // TMEM lane quadrant this warp may access
         const int h = (warp - 2) >> 2;       // column half of the 256-wide tile
         const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+        const uint32_t out_smem = out_base + (warp - 2) * OUT_WARP_BYTES;
+        uint32_t store_iter = 0;
         uint32_t chunk_iter = 0;
         bool ok = true;
         for (int64_t t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
@@ -338,44 +426,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (lane == 0) mbar_arrive(acce_bar(buf));
             }
             if (!ok) break;
-            const int64_t row = mt * BM + q * 32 + lane;
-            if (row >= p.m) continue;
-            const int64_t col0 = nt * BN + h * 128;
-            if constexpr (kRawInt32) {
-                int32_t *dst = p.a + row * p.ldy + col0;
-#pragma unroll
-                for (int j = 0; j < 128; j += 4) {
-                    if (col0 + j + 3 < p.n) {
-                        *reinterpret_cast<int4 *>(dst + j) = make_int4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            if (col0 + j + e < p.n) dst[j + e] = acc[j + e];
-                    }
-                }
-            } else {
-                const float sxr = p.sx[row];
-                float *dst = p.y + row * p.ldy + col0;
-#pragma unroll
-                for (int j = 0; j < 128; j += 4) {
-                    float v[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int64_t col = col0 + j + e;
-                        const int64_t cc = col < p.n ? col : p.n - 1;
-                        const float b = p.bias ? __ldg(p.bias + cc) : 0.0f;
-                        v[e] = fmaf(static_cast<float>(acc[j + e]) * sxr, __ldg(p.sw + cc), b);
-                    }
-                    if (col0 + j + 3 < p.n) {
-                        __stcs(reinterpret_cast<float4 *>(dst + j), make_float4(v[0], v[1], v[2], v[3]));
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            if (col0 + j + e < p.n) dst[j + e] = v[e];
-                    }
-                }
-            }
+            store_tile_rows<kRawInt32>(p, &tmY, out_smem, store_iter, mt * BM + q * 32, nt * BN + h * 128, acc, lane);
         }
+        drain_stores(lane);
         if (!ok) fail();
     }
 
@@ -387,6 +440,290 @@ __global__ void __launch_bounds__(THREADS, 1)
                      : "memory");
     }
 }
+
+
+// ---------------------------------------------------------------------------
+// CTA-pair variant (tcgen05 cta_group::2): two CTAs of a cluster compute a
+// 256 x 256 tile. Each CTA loads its own 128 rows of A and its own 128 rows
+// of B (half of the tile's N) into a 6-stage ring of 32 KB stages; the even
+// CTA of the pair issues M = 256, N = 256 MMAs that read both CTAs' shared
+// memory and write each CTA's 128 accumulator rows into that CTA's TMEM.
+// Per flop this moves two thirds of the single-CTA kernel's L2 traffic and
+// keeps six K slices in flight instead of four. The exact-chunk integer
+// accumulation and the epilogue are the same as above.
+namespace pair {
+
+constexpr int BMC = 128;  // rows of A and D per CTA (256 per pair)
+constexpr int BNP = 256;  // columns of D per pair
+constexpr int BNC = 128;  // rows of B per CTA
+constexpr int STAGES = 5;
+constexpr int A_BYTES = BMC * BK * 2;
+constexpr int B_BYTES = BNC * BK * 2;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + OUT_BYTES + BAR_BYTES;
+// kind::f16: D fp32, A and B bf16, K-major, M = 256 (both CTAs), N = 256
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(BNP >> 3) << 17) |
+                            (uint32_t(256 >> 4) << 24);
+
+__device__ __forceinline__ uint32_t cluster_rank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t local, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Tile load into this CTA's shared memory, completion counted on the even CTA's mbarrier.
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *map, int x, int y,
+                                                 uint32_t leader_bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, "
+        "{%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(leader_bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_pair(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(kIdesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive (once the issuing thread's MMAs complete) on the barrier at this offset in both CTAs.
+__device__ __forceinline__ void commit_both(uint32_t bar)
+{
+    const uint16_t mask = 0x3;
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            bar),
+        "h"(mask)
+        : "memory");
+}
+
+__device__ __forceinline__ void commit_local(uint32_t bar)
+{
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void arrive_remote(uint32_t cluster_bar)
+{
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+
+template <bool kRawInt32>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
+    gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmY, TcParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = static_cast<uint32_t>(__cvta_generic_to_shared(smem_raw));
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *gbase = smem_raw + (base - raw);
+    const uint32_t out_base = base + STAGES * STAGE_BYTES;
+    const uint32_t bars = out_base + OUT_BYTES;
+    auto full_bar = [&](int s) { return bars + 8u * s; };
+    auto empty_bar = [&](int s) { return bars + 8u * (STAGES + s); };
+    auto accf_bar = [&](int b) { return bars + 8u * (2 * STAGES + b); };
+    auto acce_bar = [&](int b) { return bars + 8u * (2 * STAGES + 2 + b); };
+    const uint32_t done_bar = bars + 8u * (2 * STAGES + 4);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + STAGES * STAGE_BYTES + OUT_BYTES + 160);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + STAGES * STAGE_BYTES + OUT_BYTES + 164);
+
+    const uint32_t rank = cluster_rank();
+    const bool leader = rank == 0;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t n_mt = (p.m + 2 * BMC - 1) / (2 * BMC), n_nt = (p.n + BNP - 1) / BNP;
+    const int64_t n_tiles = n_mt * n_nt;
+    const int64_t pair_id = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
+    const int kst = p.kstages;
+    const int n_chunks = (kst + CHUNK_KSTAGES - 1) / CHUNK_KSTAGES;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(accf_bar(b), 1);
+            mbar_init(acce_bar(b), 2 * EPI_WARPS);
+        }
+        mbar_init(done_bar, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmY)) : "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         static_cast<uint32_t>(__cvta_generic_to_shared(tmem_slot))),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    cluster_sync();  // both CTAs' barriers are initialized and TMEM is allocated before any remote use
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    auto fail = [&]() {
+        *abort_flag = 1;
+        if (p.dev_status) atomicExch(p.dev_status, static_cast<int32_t>(CONVROT_ERR_TIMEOUT));
+    };
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int issued = 0;
+            bool ok = true;
+            for (int64_t t = pair_id; t < n_tiles && ok; t += n_pairs) {
+                const int mt = static_cast<int>(t % n_mt), nt = static_cast<int>(t / n_mt);
+                const int arow = mt * 2 * BMC + static_cast<int>(rank) * BMC;
+                const int brow = nt * BNP + static_cast<int>(rank) * BNC;
+                for (int ks = 0; ks < kst; ++ks) {
+                    if (*abort_flag || !mbar_wait(empty_bar(stage), phase ^ 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t sa = base + stage * STAGE_BYTES;
+                    if (leader) mbar_arrive_expect_tx(full_bar(stage), 2 * STAGE_BYTES);
+                    const uint32_t lbar = map_to_rank(full_bar(stage), 0);
+                    tma_load_2d_pair(sa, &tmA, ks * BK, arow, lbar);
+                    tma_load_2d_pair(sa + A_BYTES, &tmB, ks * BK, brow, lbar);
+                    ++issued;
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                fail();
+                if (leader) {
+                    // both CTAs' copies for the stages armed here land before shared memory goes away
+                    for (int i = 0; i < STAGES && i < issued; ++i) {
+                        if (--stage < 0) {
+                            stage = STAGES - 1;
+                            phase ^= 1u;
+                        }
+                        mbar_wait(full_bar(stage), phase);
+                    }
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (leader && lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t chunk_iter = 0;
+            bool ok = true;
+            for (int64_t t = pair_id; t < n_tiles && ok; t += n_pairs) {
+                for (int c = 0; c < n_chunks && ok; ++c, ++chunk_iter) {
+                    const uint32_t buf = chunk_iter & 1u;
+                    if (*abort_flag || !mbar_wait(acce_bar(buf), ((chunk_iter >> 1) & 1u) ^ 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem_base + buf * BNP;
+                    const int ks0 = c * CHUNK_KSTAGES;
+                    const int ks1 = ks0 + CHUNK_KSTAGES < kst ? ks0 + CHUNK_KSTAGES : kst;
+                    for (int ks = ks0; ks < ks1; ++ks) {
+                        if (*abort_flag || !mbar_wait(full_bar(stage), phase)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t sa = base + stage * STAGE_BYTES;
+                        const uint64_t da = smem_desc(sa), db = smem_desc(sa + A_BYTES);
+#pragma unroll
+                        for (int kk = 0; kk < BK / UMMA_K; ++kk)
+                            mma_pair(d_tmem, da + 2u * kk, db + 2u * kk, (ks > ks0 || kk > 0) ? 1u : 0u);
+                        commit_both(empty_bar(stage));  // frees this stage in both CTAs once the MMAs finish
+                        if (++stage == STAGES) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
+                    if (!ok) break;
+                    commit_both(accf_bar(buf));
+                }
+            }
+            if (!ok) fail();
+            commit_local(done_bar);
+            mbar_wait(done_bar, 0);
+        }
+        __syncwarp();
+    } else {
+        const int q = warp & 3;
+        const int h = (warp - 2) >> 2;
+        const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+        const uint32_t out_smem = out_base + (warp - 2) * OUT_WARP_BYTES;
+        uint32_t store_iter = 0;
+        uint32_t chunk_iter = 0;
+        bool ok = true;
+        for (int64_t t = pair_id; t < n_tiles && ok; t += n_pairs) {
+            const int64_t mt = t % n_mt, nt = t / n_mt;
+            int32_t acc[128];
+#pragma unroll
+            for (int i = 0; i < 128; ++i) acc[i] = 0;
+            for (int c = 0; c < n_chunks; ++c, ++chunk_iter) {
+                const uint32_t buf = chunk_iter & 1u;
+                if (*abort_flag || !mbar_wait(accf_bar(buf), (chunk_iter >> 1) & 1u)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t taddr = tmem_base + lane_off + buf * BNP + h * 128;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    uint32_t r[32];
+                    tmem_ld32(taddr + j * 32, r);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) acc[j * 32 + i] += __float2int_rn(__uint_as_float(r[i]));
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) arrive_remote(map_to_rank(acce_bar(buf), 0));
+            }
+            if (!ok) break;
+            store_tile_rows<kRawInt32>(p, &tmY, out_smem, store_iter, mt * 2 * BMC + static_cast<int64_t>(rank) * BMC + q * 32,
+                                       nt * BNP + h * 128, acc, lane);
+        }
+        drain_stores(lane);
+        if (!ok) fail();
+    }
+
+    tc_fence_before();
+    cluster_sync();  // the pair's MMAs, drains and remote arrivals are all done
+    tc_fence_after();
+    if (warp == 1) {
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
+                     : "memory");
+    }
+}
+
+}  // namespace pair
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 {
@@ -417,6 +754,20 @@ bool make_map(CUtensorMap *map, const void *base, int64_t rows, int64_t kpad, in
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D map over the [m, ld] output (fp32 Y or int32 A), 32 x 32 boxes, 128-byte swizzle.
+bool make_out_map(CUtensorMap *map, void *base, int64_t m, int64_t n, int64_t ld, bool int32_out)
+{
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(m)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 4};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(OUT_BOX), static_cast<cuuint32_t>(OUT_BOX)};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(map, int32_out ? CU_TENSOR_MAP_DATA_TYPE_INT32 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides,
+              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int sm_count()
 {
     int dev = 0, n = 0;
@@ -433,6 +784,9 @@ cudaError_t launch_gemm_tc(const GemmArgs &g, cudaStream_t stream)
     CUtensorMap ta, tb;
     if (!make_map(&ta, g.qx, g.m, g.kpad, g.ldqx, BM) || !make_map(&tb, g.qw, g.n, g.kpad, g.ldqw, BN))
         return cudaErrorInvalidValue;
+    CUtensorMap ty;
+    if (!make_out_map(&ty, g.a ? static_cast<void *>(g.a) : static_cast<void *>(g.y), g.m, g.n, g.ldy, g.a != nullptr))
+        return cudaErrorInvalidValue;
     TcParams p{};
     p.m = g.m;
     p.n = g.n;
@@ -444,20 +798,41 @@ cudaError_t launch_gemm_tc(const GemmArgs &g, cudaStream_t stream)
     p.a = g.a;
     p.ldy = g.ldy;
     p.dev_status = g.dev_status;
-    const int64_t tiles = ((g.m + BM - 1) / BM) * ((g.n + BN - 1) / BN);
     const int sms = sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
+    if (g.m > BM) {
+        // CTA pairs: 256 x 256 tiles, half of A's rows and half of B's rows per CTA
+        CUtensorMap pa, pb;
+        if (!make_map(&pa, g.qx, g.m, g.kpad, g.ldqx, pair::BMC) || !make_map(&pb, g.qw, g.n, g.kpad, g.ldqw, pair::BNC))
+            return cudaErrorInvalidValue;
+        const int64_t tiles = ((g.m + 2 * pair::BMC - 1) / (2 * pair::BMC)) * ((g.n + pair::BNP - 1) / pair::BNP);
+        const int64_t pairs = tiles < sms / 2 ? tiles : sms / 2;
+        const unsigned grid = static_cast<unsigned>(2 * pairs);
+        if (g.a) {
+            auto k = pair::gemm_tc_pair_kernel<true>;
+            cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, pair::SMEM_BYTES);
+            if (e != cudaSuccess) return e;
+            k<<<grid, THREADS, pair::SMEM_BYTES, stream>>>(pa, pb, ty, p);
+        } else {
+            auto k = pair::gemm_tc_pair_kernel<false>;
+            cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, pair::SMEM_BYTES);
+            if (e != cudaSuccess) return e;
+            k<<<grid, THREADS, pair::SMEM_BYTES, stream>>>(pa, pb, ty, p);
+        }
+        return cudaGetLastError();
+    }
+    const int64_t tiles = ((g.m + BM - 1) / BM) * ((g.n + BN - 1) / BN);
     const unsigned grid = static_cast<unsigned>(tiles < sms ? tiles : sms);
     if (g.a) {
         auto k = gemm_tc_kernel<true>;
         cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
         if (e != cudaSuccess) return e;
-        k<<<grid, THREADS, SMEM_BYTES, stream>>>(ta, tb, p);
+        k<<<grid, THREADS, SMEM_BYTES, stream>>>(ta, tb, ty, p);
     } else {
         auto k = gemm_tc_kernel<false>;
         cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
         if (e != cudaSuccess) return e;
-        k<<<grid, THREADS, SMEM_BYTES, stream>>>(ta, tb, p);
+        k<<<grid, THREADS, SMEM_BYTES, stream>>>(ta, tb, ty, p);
     }
     return cudaGetLastError();
 }

@@ -33,14 +33,15 @@
 // (butterflies by warp shuffle) and the rest from the slot (register
 // butterflies). The float4 component is digit 0 of the in-group index.
 //
-// Two kernels share this arithmetic:
-//   pack_ring_kernel  persistent, one CTA per SM; whole rows stream into a
-//                     shared-memory ring by bulk copies (cp.async.bulk) with
-//                     mbarrier completion, several stages ahead of the math.
-//   pack_direct_kernel rows too long for the ring: registers are loaded from
-//                     global memory directly and a thread-block cluster may
-//                     own one row (absmax exchanged through distributed
-//                     shared memory).
+// Launch shape. One kernel, loading registers straight from global memory
+// with streaming 16-byte loads: a CTA of about 128 threads owns whole rows
+// (96 threads per row at K = 3072), and many CTAs per SM overlap their
+// load / compute / store phases. Rows longer than 512 threads hold are split
+// over a thread-block cluster, whose CTAs exchange their partial row maxima
+// through distributed shared memory. (Persistent variants that stream rows
+// through a shared-memory ring with bulk copies, with or without a
+// shared-memory transpose in place of the lane shuffles, measured no faster
+// on any of the DiT shapes, so they were dropped.)
 #include <cuda_bf16.h>
 
 #include "../../include/convrot.h"
@@ -51,8 +52,6 @@ namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
 constexpr uint32_t kSign = 0x80000000u;
-constexpr int kMaxStages = 4;
-constexpr uint64_t kTimeoutNs = 4000000000ull;  // 4 s
 
 template <int S>
 constexpr int kMaxThreads = S >= 32 ? 256 : 512;
@@ -82,38 +81,6 @@ __device__ __forceinline__ float round_half_away(float v)
     return copysignf(truncf(__fadd_rz(fabsf(v), 0.5f)), v);
 }
 
-__device__ __forceinline__ uint64_t globaltimer()
-{
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
-{
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer();
-    for (;;) {
-#pragma unroll 1
-        for (int i = 0; i < 32; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
-        if (globaltimer() - t0 > kTimeoutNs) return false;
-    }
-}
-
 __device__ __forceinline__ uint32_t cluster_smem_addr(const void *p, uint32_t rank)
 {
     uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -135,26 +102,39 @@ __device__ __forceinline__ void cluster_sync_all()
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// Where one thread's slots sit along a row.
+// Where one thread's slots sit along a row, and everything about them that
+// is the same for every row the thread handles: which slots hold data, the
+// sign of D at each slot, and how far Pi moves each slot's output.
 template <int LANES, int S>
 struct Place {
-    int l_in;        // lane inside the tile
-    int64_t q0;      // quad index of slot 0
-    int lbg, sbg;    // lane / slot bits inside a group
-    uint32_t gmask;  // in-group quad-index mask
-    int qbits;
+    int l_in;          // lane inside the tile
+    int q0;            // quad index of slot 0 along the row
+    int lbg, sbg;      // lane / slot bits inside a group
+    int qbits;         // in-group quad-index bits (2n - 2)
+    uint32_t valid;    // bit j: slot j holds data (quad < k/4)
+    uint32_t sgn[S];   // sign of D at slot j (0 or kSign), digit 0 excluded
+    int delta[S];      // Pi: output quad = input quad + delta[j]
 
-    __device__ __forceinline__ Place(int t_row, int n)
+    __device__ __forceinline__ Place(int t_row, int n, int kq)
     {
         l_in = t_row & ((1 << LANES) - 1);
-        q0 = static_cast<int64_t>(t_row >> LANES) * (S << LANES) + l_in;
+        q0 = (t_row >> LANES) * (S << LANES) + l_in;
         qbits = 2 * n - 2;
         lbg = qbits < LANES ? qbits : LANES;
         sbg = qbits - lbg;
-        gmask = (1u << qbits) - 1u;
+        const uint32_t gmask = (1u << qbits) - 1u;
+        valid = 0;
+#pragma unroll
+        for (int j = 0; j < S; ++j) {
+            const int q = quad(j);
+            if (q < kq) valid |= 1u << j;
+            // a tile is a whole number of groups, so the in-group index depends on (lane, slot) only
+            const uint32_t g = static_cast<uint32_t>(q) & gmask;
+            sgn[j] = quad_sign(g);
+            delta[j] = static_cast<int>(swap_digit_bits(g, qbits)) - static_cast<int>(g);
+        }
     }
-    __device__ __forceinline__ int64_t quad(int j) const { return q0 + static_cast<int64_t>(j) * (1 << LANES); }
-    __device__ __forceinline__ uint32_t group_index(int j) const { return static_cast<uint32_t>(quad(j)) & gmask; }
+    __device__ __forceinline__ int quad(int j) const { return q0 + j * (1 << LANES); }
 };
 
 // D, then the Walsh-Hadamard butterflies over all 2n in-group bits.
@@ -163,7 +143,7 @@ __device__ __forceinline__ void rotate(float4 (&v)[S], const Place<LANES, S> &pl
 {
 #pragma unroll
     for (int j = 0; j < S; ++j) {
-        const uint32_t sg = quad_sign(pl.group_index(j));
+        const uint32_t sg = pl.sgn[j];
         v[j].x = xor_sign(v[j].x, sg);
         v[j].y = xor_sign(v[j].y, sg);
         v[j].z = xor_sign(v[j].z, sg);
@@ -210,25 +190,23 @@ __device__ __forceinline__ float absmax(const float4 (&v)[S])
 
 // Codes of one thread's slots, written to their Pi-permuted places (D folded into inv).
 template <int LANES, int S, bool kBf16>
-__device__ __forceinline__ void quantize_store(const float4 (&v)[S], const Place<LANES, S> &pl, char *qrow, int kq,
+__device__ __forceinline__ void quantize_store(const float4 (&v)[S], const Place<LANES, S> &pl, char *qrow,
                                                float inv)
 {
 #pragma unroll
     for (int j = 0; j < S; ++j) {
-        const int64_t q = pl.quad(j);
-        if (q >= kq) continue;
-        const uint32_t g = pl.group_index(j);
-        const int64_t q_out = q - g + swap_digit_bits(g, pl.qbits);
-        const float ip = xor_sign(inv, quad_sign(g)), in = xor_sign(ip, kSign);
+        if (!(pl.valid & (1u << j))) continue;
+        const int q_out = pl.quad(j) + pl.delta[j];
+        const float ip = xor_sign(inv, pl.sgn[j]), in = xor_sign(ip, kSign);
         // Pi on digit 0: components 1 and 2 trade places
         const float r0 = round_half_away(v[j].x * ip);
         const float r1 = round_half_away(v[j].z * ip);
         const float r2 = round_half_away(v[j].y * ip);
         const float r3 = round_half_away(v[j].w * in);
         if constexpr (kBf16) {
-            // |r| <= 127: the bf16 of r is the top half of its fp32 bits (+0 turns -0 into 0)
-            const uint32_t lo = __byte_perm(__float_as_uint(r0 + 0.0f), __float_as_uint(r1 + 0.0f), 0x7632);
-            const uint32_t hi = __byte_perm(__float_as_uint(r2 + 0.0f), __float_as_uint(r3 + 0.0f), 0x7632);
+            // |r| <= 127: the bf16 of r is the top half of its fp32 bits (a zero code may be -0)
+            const uint32_t lo = __byte_perm(__float_as_uint(r0), __float_as_uint(r1), 0x7632);
+            const uint32_t hi = __byte_perm(__float_as_uint(r2), __float_as_uint(r3), 0x7632);
             reinterpret_cast<uint2 *>(qrow)[q_out] = make_uint2(lo, hi);
         } else {
             // r + 1.5 * 2^23 holds r in its low mantissa bits: the low byte is r as int8
@@ -261,113 +239,6 @@ __device__ __forceinline__ float scale_of(float amax_unnorm, int n, float *inv)
     return s;
 }
 
-struct RingPlan {
-    int threads_per_row;  // multiple of 2^LANES; rows_per_stage * threads_per_row = blockDim.x
-    int rows_per_stage;
-    int stages;
-    uint32_t row_bytes;    // k * 4
-    uint32_t stage_bytes;  // rows_per_stage * row_bytes, rounded up to 128
-};
-
-template <int LANES, int S, bool kBf16>
-__global__ void __launch_bounds__(kMaxThreads<S>) pack_ring_kernel(PackArgs a, RingPlan P)
-{
-    extern __shared__ __align__(128) uint8_t ring[];
-    __shared__ __align__(8) uint64_t full_bar[kMaxStages];
-    __shared__ float part[2][kMaxThreads<S>];
-
-    const int lane = threadIdx.x & 31;
-    const int tpr = P.threads_per_row, R = P.rows_per_stage, NS = P.stages;
-    const int r_local = threadIdx.x / tpr;
-    const int t_row = threadIdx.x - r_local * tpr;
-    const int n = a.log4g;
-    const int kq = a.k >> 2, kpq = a.kpad >> 2;
-    const Place<LANES, S> pl(t_row, n);
-    const int64_t nblocks = (a.rows + R - 1) / R;
-    const uint32_t ring_base = static_cast<uint32_t>(__cvta_generic_to_shared(ring));
-    const uint32_t bar_base = static_cast<uint32_t>(__cvta_generic_to_shared(full_bar));
-    const int seg = (tpr & 31) == 0 ? 32 : (tpr & -tpr);  // power of two dividing tpr, <= 32
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < NS; ++s)
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar_base + 8u * s) : "memory");
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    __syncthreads();
-
-    // one bulk copy per row of the block into the stage; completion counted in bytes on its mbarrier
-    auto issue = [&](int stage, int64_t blk) {
-        if (blk >= nblocks) return;
-        const int64_t r0 = blk * R;
-        const int nr = a.rows - r0 < R ? static_cast<int>(a.rows - r0) : R;
-        const uint32_t bar = bar_base + 8u * stage;
-        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
-                     "r"(static_cast<uint32_t>(nr) * P.row_bytes)
-                     : "memory");
-        for (int i = 0; i < nr; ++i) {
-            const float *src = a.x + (r0 + i) * a.ldx;
-            asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                             ring_base + stage * P.stage_bytes + i * P.row_bytes),
-                         "l"(src), "r"(P.row_bytes), "r"(bar)
-                         : "memory");
-        }
-    };
-
-    if (threadIdx.x == 0)
-        for (int s = 0; s < NS - 1; ++s) issue(s, blockIdx.x + static_cast<int64_t>(s) * gridDim.x);
-
-    int it = 0;
-    bool ok = true;
-    for (int64_t blk = blockIdx.x; blk < nblocks; blk += gridDim.x, ++it) {
-        const int stage = it % NS;
-        if (threadIdx.x == 0) {
-            // the stage refilled here was read into registers before the previous barrier
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            issue((it + NS - 1) % NS, blk + static_cast<int64_t>(NS - 1) * gridDim.x);
-        }
-        const bool got = mbar_wait(bar_base + 8u * stage, static_cast<uint32_t>(it / NS) & 1u);
-
-        const int64_t row = blk * R + r_local;
-        const bool row_ok = got && row < a.rows;
-        const float4 *src = reinterpret_cast<const float4 *>(ring + stage * P.stage_bytes + r_local * P.row_bytes);
-        float4 v[S];
-#pragma unroll
-        for (int j = 0; j < S; ++j) {
-            const int64_t q = pl.quad(j);
-            v[j] = (row_ok && q < kq) ? src[q] : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-        rotate<LANES, S>(v, pl);
-
-        float m = absmax<S>(v);
-        for (int off = seg >> 1; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, off));
-        float *pp = part[it & 1];
-        if ((lane & (seg - 1)) == 0) pp[threadIdx.x / seg] = m;
-        // all threads agree on whether the stage arrived; a failed wait ends the loop everywhere
-        if (!__syncthreads_and(got)) {
-            ok = false;
-            break;
-        }
-        float amax = 0.0f;
-        const int p0 = (r_local * tpr) / seg, np = tpr / seg;
-        for (int i = 0; i < np; ++i) amax = fmaxf(amax, pp[p0 + i]);
-        float inv;
-        const float s = scale_of(amax, n, &inv);
-        if (row < a.rows) {
-            if (t_row == 0) a.scale[row] = s;
-            char *qrow = static_cast<char *>(a.q) + row * a.ldq * (kBf16 ? 2 : 1);
-            quantize_store<LANES, S, kBf16>(v, pl, qrow, kq, inv);
-            zero_pad<kBf16>(qrow, kq, kpq, t_row, tpr);
-        }
-    }
-    if (!ok && threadIdx.x == 0) {
-        if (a.dev_status) atomicExch(a.dev_status, static_cast<int32_t>(CONVROT_ERR_TIMEOUT));
-        // let the copies already issued land before the CTA's shared memory goes away
-        int64_t blk = blockIdx.x + static_cast<int64_t>(it) * gridDim.x;
-        for (int s = 0; s < NS; ++s, blk += gridDim.x)
-            if (blk < nblocks) mbar_wait(bar_base + 8u * ((it + s) % NS), static_cast<uint32_t>((it + s) / NS) & 1u);
-    }
-}
-
 struct DirectPlan {
     int threads_per_row;  // per CTA
     int rows_per_cta;
@@ -375,7 +246,7 @@ struct DirectPlan {
 };
 
 template <int LANES, int S, bool kBf16>
-__global__ void __launch_bounds__(kMaxThreads<S>) pack_direct_kernel(PackArgs a, DirectPlan L, int64_t row0)
+__global__ void __launch_bounds__(kMaxThreads<S>) pack_kernel(PackArgs a, DirectPlan L, int64_t row0)
 {
     const int lane = threadIdx.x & 31;
     const int cl = L.cl;
@@ -389,15 +260,13 @@ __global__ void __launch_bounds__(kMaxThreads<S>) pack_direct_kernel(PackArgs a,
     const int t_row = cr * tpr + t_cta;
     const int n = a.log4g;
     const int kq = a.k >> 2, kpq = a.kpad >> 2;
-    const Place<LANES, S> pl(t_row, n);
+    const Place<LANES, S> pl(t_row, n, kq);
 
     const float4 *src = reinterpret_cast<const float4 *>(a.x + (row_ok ? row : 0) * a.ldx);
     float4 v[S];
 #pragma unroll
-    for (int j = 0; j < S; ++j) {
-        const int64_t q = pl.quad(j);
-        v[j] = (row_ok && q < kq) ? __ldcs(src + q) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
+    for (int j = 0; j < S; ++j)
+        v[j] = (row_ok && (pl.valid & (1u << j))) ? __ldcs(src + pl.quad(j)) : make_float4(0.f, 0.f, 0.f, 0.f);
     rotate<LANES, S>(v, pl);
 
     float m = absmax<S>(v);
@@ -423,7 +292,7 @@ __global__ void __launch_bounds__(kMaxThreads<S>) pack_direct_kernel(PackArgs a,
     if (row_ok) {
         if (t_row == 0) a.scale[row] = s;
         char *qrow = static_cast<char *>(a.q) + row * a.ldq * (kBf16 ? 2 : 1);
-        quantize_store<LANES, S, kBf16>(v, pl, qrow, kq, inv);
+        quantize_store<LANES, S, kBf16>(v, pl, qrow, inv);
         zero_pad<kBf16>(qrow, kq, kpq, t_row, tpr * cl);
     }
     if (cl > 1) cluster_sync_all();  // no CTA leaves while another may still read its cta_max
@@ -457,29 +326,6 @@ int threads_per_row(const Shape &sh, int k)
     return tiles << sh.lanes;
 }
 
-constexpr uint32_t kStageTarget = 64 * 1024;
-constexpr uint32_t kRingBytes = 200 * 1024;
-
-// Ring plan, or stages == 0 when rows are too long for it.
-RingPlan ring_plan(const Shape &sh, int k)
-{
-    RingPlan P{};
-    const int T = threads_per_row(sh, k);
-    const int max_threads = sh.S >= 32 ? 256 : 512;
-    const int step = 32 / gcd_int(T, 32);  // rows per stage must fill whole warps
-    P.row_bytes = static_cast<uint32_t>(k) * 4u;
-    if (step * T > max_threads || static_cast<uint64_t>(step) * P.row_bytes > kStageTarget) return P;
-    int R = step;
-    while ((R + step) * T <= max_threads && static_cast<uint64_t>(R + step) * P.row_bytes <= kStageTarget) R += step;
-    P.threads_per_row = T;
-    P.rows_per_stage = R;
-    P.stage_bytes = (R * P.row_bytes + 127u) & ~127u;
-    int ns = static_cast<int>(kRingBytes / P.stage_bytes);
-    P.stages = ns > kMaxStages ? kMaxStages : ns;
-    if (P.stages < 2) P.stages = 0;
-    return P;
-}
-
 DirectPlan direct_plan(const Shape &sh, int k)
 {
     const int T = threads_per_row(sh, k);
@@ -490,7 +336,7 @@ DirectPlan direct_plan(const Shape &sh, int k)
         L.cl = 1;
         L.threads_per_row = T;
         int R = step;
-        while (R * T < 256 && (R + step) * T <= max_threads) R += step;
+        while (R * T < 128 && (R + step) * T <= max_threads) R += step;
         L.rows_per_cta = R;
     } else if (T <= max_threads) {
         L.cl = 1;
@@ -508,31 +354,10 @@ DirectPlan direct_plan(const Shape &sh, int k)
     return L;
 }
 
-int sm_count()
-{
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    return n;
-}
-
 template <int LANES, int S, bool kBf16>
 cudaError_t launch_shape(const PackArgs &a, cudaStream_t stream)
 {
     const Shape sh{LANES, S};
-    const RingPlan P = ring_plan(sh, a.k);
-    if (P.stages > 0) {
-        auto kern = pack_ring_kernel<LANES, S, kBf16>;
-        const int smem = static_cast<int>(P.stages * P.stage_bytes);
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        const int64_t nblocks = (a.rows + P.rows_per_stage - 1) / P.rows_per_stage;
-        const int sms = sm_count();
-        if (sms <= 0) return cudaErrorInvalidDevice;
-        const int64_t grid = nblocks < sms ? nblocks : sms;
-        kern<<<static_cast<unsigned>(grid), P.threads_per_row * P.rows_per_stage, smem, stream>>>(a, P);
-        return cudaGetLastError();
-    }
     const DirectPlan L = direct_plan(sh, a.k);
     if (L.cl > 16) return cudaErrorInvalidConfiguration;
     const int64_t row_blocks = (a.rows + L.rows_per_cta - 1) / L.rows_per_cta;
@@ -551,7 +376,7 @@ cudaError_t launch_shape(const PackArgs &a, cudaStream_t stream)
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        auto kern = pack_direct_kernel<LANES, S, kBf16>;
+        auto kern = pack_kernel<LANES, S, kBf16>;
         if (L.cl > 8) {
             cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
             if (e != cudaSuccess) return e;
@@ -562,12 +387,13 @@ cudaError_t launch_shape(const PackArgs &a, cudaStream_t stream)
     return cudaSuccess;
 }
 
+
 template <bool kBf16>
 cudaError_t dispatch(const PackArgs &a, cudaStream_t stream)
 {
-    if (a.log4g <= 4) return launch_shape<3, 8, kBf16>(a, stream);
-    if (a.log4g == 5) return launch_shape<5, 8, kBf16>(a, stream);
-    if (a.log4g == 6) return launch_shape<5, 32, kBf16>(a, stream);
+    if (a.log4g <= 4) return launch_shape<3, 8, kBf16>(a, stream);   // G <= 256
+    if (a.log4g == 5) return launch_shape<5, 8, kBf16>(a, stream);   // G = 1024
+    if (a.log4g == 6) return launch_shape<5, 32, kBf16>(a, stream);  // G = 4096
     return cudaErrorInvalidValue;
 }
 
