@@ -165,6 +165,7 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32])
 
 struct TcParams {
     int64_t m, n;
+    int32_t vec_cols;  // s_w and bias are 16-byte aligned
     int32_t kstages;  // kpad / BK
     const float *sx, *sw, *bias;
     float *y;
@@ -215,16 +216,27 @@ __device__ __forceinline__ void store_tile_rows(const TcParams &p, const CUtenso
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
             uint32_t w[4];
+            float4 sw4 = make_float4(0.f, 0.f, 0.f, 0.f), b4 = make_float4(0.f, 0.f, 0.f, 0.f);
+            if constexpr (!kRawInt32) {
+                const int64_t col = x + c * 4;
+                if (p.vec_cols) {  // s_w and bias 16-byte aligned: 4 columns per load
+                    sw4 = __ldg(reinterpret_cast<const float4 *>(p.sw + col));
+                    if (p.bias) b4 = __ldg(reinterpret_cast<const float4 *>(p.bias + col));
+                } else {
+                    sw4 = make_float4(__ldg(p.sw + col), __ldg(p.sw + col + 1), __ldg(p.sw + col + 2), __ldg(p.sw + col + 3));
+                    if (p.bias)
+                        b4 = make_float4(__ldg(p.bias + col), __ldg(p.bias + col + 1), __ldg(p.bias + col + 2),
+                                         __ldg(p.bias + col + 3));
+                }
+            }
+            const float swv[4] = {sw4.x, sw4.y, sw4.z, sw4.w}, bv[4] = {b4.x, b4.y, b4.z, b4.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int j = cc * 32 + c * 4 + e;
-                if constexpr (kRawInt32) {
+                if constexpr (kRawInt32)
                     w[e] = static_cast<uint32_t>(acc[j]);
-                } else {
-                    const int64_t col = x + c * 4 + e;
-                    const float b = p.bias ? __ldg(p.bias + col) : 0.0f;
-                    w[e] = __float_as_uint(fmaf(static_cast<float>(acc[j]) * sxr, __ldg(p.sw + col), b));
-                }
+                else
+                    w[e] = __float_as_uint(fmaf(static_cast<float>(acc[j]) * sxr, swv[e], bv[e]));
             }
             const uint32_t addr = buf + lane * (OUT_BOX * 4) + ((c ^ (lane & 7)) << 4);
             asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[0]), "r"(w[1]), "r"(w[2]),
@@ -798,6 +810,7 @@ cudaError_t launch_gemm_tc(const GemmArgs &g, cudaStream_t stream)
     p.a = g.a;
     p.ldy = g.ldy;
     p.dev_status = g.dev_status;
+    p.vec_cols = (reinterpret_cast<uintptr_t>(g.sw) % 16 == 0) && (reinterpret_cast<uintptr_t>(g.bias) % 16 == 0);
     const int sms = sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
     if (g.m > BM) {
