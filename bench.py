@@ -218,16 +218,18 @@ def run_ours(args):
 
     # inputs: every rank runs the full workload on its own GPU (weak scaling; rows are independent)
     X = torch.from_numpy(inputs.activations(wl)).to(dev)
-    W = torch.from_numpy(inputs.weights(wl)).to(dev)
-    b = torch.from_numpy(inputs.bias(wl)).to(dev)
-    touched = wl.m * wl.k * 4 + wl.n * wl.k * (1 if codes == cr.CODES_I8 else 2) + wl.m * wl.n * 4
+    # linears sharing the packed input (q, k, v) run as one grouped GEMM over concatenated weights
+    Ws = [torch.from_numpy(inputs.weights(wl, i)).to(dev) for i in range(wl.linears)]
+    b = torch.from_numpy(np.concatenate([inputs.bias(wl, i) for i in range(wl.linears)])).to(dev)
+    n_all = wl.n * wl.linears
+    touched = wl.m * wl.k * 4 + n_all * wl.k * (1 if codes == cr.CODES_I8 else 2) + wl.m * n_all * 4
     R = max(2, -(-3 * L2_BYTES // touched) + 1)  # rotating sets so a reuse is > 2 L2s away
     R = min(R, 6)
     Xs = [X] + [X.clone() for _ in range(R - 1)]
-    pws = [cr.convrot_quantize_weights(W, wl.G, codes) for _ in range(R)]
+    pws = [cr.quantize_weights_grouped(Ws, wl.G, codes) for _ in range(R)]
     pxs = [cr.empty_packed(wl.m, wl.k, codes, dev) for _ in range(R)]
-    Ys = [torch.empty((wl.m, wl.n), dtype=torch.float32, device=dev) for _ in range(R)]
-    del W
+    Ys = [torch.empty((wl.m, n_all), dtype=torch.float32, device=dev) for _ in range(R)]
+    del Ws
     stream = torch.cuda.current_stream(dev)
 
     def step(i, ev=None):
@@ -284,7 +286,7 @@ def run_ours(args):
     # end to end through the public API: pinned host X in, pinned host Y out, every step
     e2e_steps = max(3, min(args.steps, 10))
     Xh = torch.from_numpy(inputs.activations(wl)).pin_memory()
-    Yh = torch.empty((wl.m, wl.n), dtype=torch.float32).pin_memory()
+    Yh = torch.empty((wl.m, n_all), dtype=torch.float32).pin_memory()
     Xd = torch.empty_like(Xs[0])
 
     def e2e_step():
@@ -311,7 +313,7 @@ def run_ours(args):
         pg.all_reduce(t, op=pg.ReduceOp.MAX)
         ms_step, e2e_ms = float(t[0]), float(t[1])
 
-    ops = float(wl.int_ops)
+    ops = float(wl.int_ops) * wl.linears
     value = world * ops / (ms_step * 1e-3) / 1e12
     gemm_avg = sum(gemm_ms) / len(gemm_ms)
     pack_avg = sum(pack_ms) / len(pack_ms)
@@ -328,7 +330,8 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "s8" if codes == cr.CODES_I8 else "bf16-coded s8",
         "data": "synthetic (seeded N(0,1) activations with 0.1% outlier channels x50, N(0,0.02^2) weights)",
-        "config": {"workload": f"{wl.name} M{wl.m} K{wl.k} N{wl.n} G{wl.G}", "global_batch": wl.m * world,
+        "config": {"workload": f"{wl.name} M{wl.m} K{wl.k} N{wl.n}" + (f"x{wl.linears} (one grouped GEMM)" if wl.linears > 1 else "")
+                   + f" G{wl.G}", "global_batch": wl.m * world,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "codes": "i8" if codes == cr.CODES_I8 else "bf16",
                    "l2": f"{R} rotating input/output sets, {touched / 1e6:.0f} MB touched per step (> L2)"},
@@ -340,7 +343,7 @@ def run_ours(args):
                           "frac": pack_gbs / pk["hbm_gbs"], "bytes_per_launch": pack_bytes,
                           "peak_source": f"{pk['source']} copy bandwidth"},
         "e2e": {"value": world * ops / (e2e_ms * 1e-3) / 1e12, "unit": "TOPS",
-                "h2d_bytes_per_step": wl.m * wl.k * 4, "d2h_bytes_per_step": wl.m * wl.n * 4,
+                "h2d_bytes_per_step": wl.m * wl.k * 4, "d2h_bytes_per_step": wl.m * n_all * 4,
                 "ms_per_step": e2e_ms},
         "gpu_launches": 2 * args.steps,
         "clocks": clk,

@@ -206,6 +206,42 @@ def convrot_gemm_i32(x: Packed, w: Packed, out: torch.Tensor | None = None,
     return out
 
 
+def quantize_weights_grouped(Ws, G: int, codes: int = CODES_I8, stream=None) -> Packed:
+    """Quantize several weights that will multiply the same packed input into one packed block.
+
+    Row block i of the result holds W_i's codes and scales (each W_i quantized by
+    the same kernel as convrot_quantize_weights, written in place). One
+    convrot_linear against it computes every linear at once; its output
+    [m, sum(n_i)] holds linear i in columns [off_i, off_i + n_i) -- the page's
+    packed activation is reused by all of them ("Runtime activation quantization").
+    """
+    Ws = list(Ws)
+    if not Ws:
+        raise ValueError("no weights")
+    k = Ws[0].shape[1]
+    if any(W.shape[1] != k for W in Ws):
+        raise ValueError("grouped weights need the same input features")
+    rows = sum(W.shape[0] for W in Ws)
+    out = empty_packed(rows, k, codes, Ws[0].device)
+    r0 = 0
+    for W in Ws:
+        n = W.shape[0]
+        part = Packed(out.q[r0:r0 + n], out.scale[r0:r0 + n], n, k, 0, codes)
+        convrot_quantize_weights(W, G, codes, out=part, stream=stream)
+        r0 += n
+    out.group_size = int(G)
+    return out
+
+
+def split_columns(Y: torch.Tensor, sizes):
+    """Views of the column blocks of a grouped linear's output."""
+    views, c0 = [], 0
+    for n in sizes:
+        views.append(Y[:, c0:c0 + n])
+        c0 += n
+    return views
+
+
 def packed_from_codes(q_int8: torch.Tensor, scale: torch.Tensor, group_size: int, codes: int = CODES_I8) -> Packed:
     """Wraps externally produced codes (e.g. a checkpoint's I8 weight and its scales) as a Packed.
 

@@ -80,15 +80,16 @@ def activations(wl: Workload, rows: slice | None = None) -> np.ndarray:
     return X if rows is None else np.ascontiguousarray(X[rows])
 
 
-def weights(wl: Workload) -> np.ndarray:
-    """W fp32 [N, K] ~ N(0, 0.02^2)."""
-    return (_rng(wl.seed, _TAG_W).standard_normal((wl.n, wl.k), dtype=np.float32)
-            * np.float32(0.02))
+def weights(wl: Workload, index: int = 0) -> np.ndarray:
+    """W fp32 [N, K] ~ N(0, 0.02^2); `index` picks one of the linears sharing the input."""
+    rng = _rng(wl.seed, _TAG_W) if index == 0 else np.random.default_rng(list(wl.seed) + [_TAG_W, index])
+    return rng.standard_normal((wl.n, wl.k), dtype=np.float32) * np.float32(0.02)
 
 
-def bias(wl: Workload) -> np.ndarray:
+def bias(wl: Workload, index: int = 0) -> np.ndarray:
     """b fp32 [N] ~ N(0, 0.01^2)."""
-    return _rng(wl.seed, _TAG_B).standard_normal((wl.n,), dtype=np.float32) * np.float32(0.01)
+    rng = _rng(wl.seed, _TAG_B) if index == 0 else np.random.default_rng(list(wl.seed) + [_TAG_B, index])
+    return rng.standard_normal((wl.n,), dtype=np.float32) * np.float32(0.01)
 
 
 def _sweep(G: int) -> Workload:

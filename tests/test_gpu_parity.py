@@ -259,3 +259,44 @@ def test_full_size_sampled(name):
     A_ref = oracle.gemm_i32(Qx_ref, Qw_ref, wl.k)
     _, Y64_ref = oracle.reconstruct(A_ref, sx_ref, sw_ref, b)
     parity.check_y_end_to_end(Y_rows, Y64_ref)
+
+
+def test_grouped_linears_share_one_pack():
+    """q, k, v against one packed input in one GEMM equal three separate linears bit for bit."""
+    rng = np.random.default_rng(31)
+    m, k, sizes = 300, 512, (256, 384, 200)
+    X = rng.standard_normal((m, k)).astype(np.float32)
+    Ws = [(0.02 * rng.standard_normal((n, k))).astype(np.float32) for n in sizes]
+    bs = [rng.standard_normal(n).astype(np.float32) for n in sizes]
+    px = cr.convrot_pack_activations(to_dev(X), 64, cr.CODES_BF16)
+    pw = cr.quantize_weights_grouped([to_dev(W) for W in Ws], 64, cr.CODES_BF16)
+    Y = cr.convrot_linear(px, pw, to_dev(np.concatenate(bs)))
+    singles = []
+    for W, b in zip(Ws, bs):
+        p1 = cr.convrot_quantize_weights(to_dev(W), 64, cr.CODES_BF16)
+        singles.append(cr.convrot_linear(px, p1, to_dev(b)))
+    torch.cuda.synchronize()
+    for view, single in zip(cr.split_columns(Y, sizes), singles):
+        assert torch.equal(view, single)
+    # and against the oracle, end to end
+    ref = oracle.linear(X, np.concatenate(Ws), np.concatenate(bs), 64)
+    parity.check_y_end_to_end(Y.cpu().numpy(), ref["Y64"])
+
+
+@pytest.mark.slow
+def test_full_size_attention_grouped_qkv():
+    """The attention workload as the bench runs it: one pack, q/k/v in one grouped GEMM."""
+    wl = inputs.WORKLOADS["attn_qkv"]
+    X = inputs.activations(wl)
+    Ws = [inputs.weights(wl, i) for i in range(3)]
+    bs = [inputs.bias(wl, i) for i in range(3)]
+    px = cr.convrot_pack_activations(to_dev(X), wl.G, cr.CODES_BF16)
+    pw = cr.quantize_weights_grouped([to_dev(W) for W in Ws], wl.G, cr.CODES_BF16)
+    Y = cr.convrot_linear(px, pw, to_dev(np.concatenate(bs)))
+    torch.cuda.synchronize()
+    rows = np.concatenate([np.random.default_rng(5).choice(wl.m - 8, 48, replace=False), np.arange(wl.m - 8, wl.m)])
+    Qx_ref, sx_ref, vx = oracle.pack_rows(X[rows], wl.G)
+    Qw_ref, sw_ref, _ = oracle.pack_rows(np.concatenate(Ws), wl.G, want_pre_round=False)
+    A_ref = oracle.gemm_i32(Qx_ref, Qw_ref, wl.k)
+    _, Y64 = oracle.reconstruct(A_ref, sx_ref, sw_ref, np.concatenate(bs))
+    parity.check_y_end_to_end(Y[torch.from_numpy(rows).cuda()].cpu().numpy(), Y64)
