@@ -121,8 +121,9 @@ convrot_status convrot_quantize_weights(const float *W, int64_t n, int64_t k, in
  *   m      rows (tokens), m >= 0 (0: nothing is launched).
  *   k, G   as for convrot_quantize_weights.
  *   out_x  caller-filled q/scale/ldq/codes; receives rows = m, k, G.
- *   dev_status  device int32 or NULL; see convrot_linear. (The pack kernel
- *               has no bounded waits today and leaves it untouched.)
+ *   dev_status  device int32 or NULL; see convrot_linear. (For G <= 256 the
+ *               pack streams rows into shared memory with bulk copies and
+ *               waits for them with a 4 s bound; the other forms never wait.)
  */
 convrot_status convrot_pack_activations(const float *X, int64_t m, int64_t k, int64_t ldx,
                                         int32_t G, convrot_packed *out_x, int32_t *dev_status,

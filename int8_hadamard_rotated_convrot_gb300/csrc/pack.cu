@@ -298,16 +298,348 @@ __global__ void __launch_bounds__(kMaxThreads<S>) pack_kernel(PackArgs a, Direct
     if (cl > 1) cluster_sync_all();  // no CTA leaves while another may still read its cta_max
 }
 
+// ---------------------------------------------------------------------------
+// Groups of up to 256 (n <= 4, every DiT shape): a fixed layout known at
+// compile time.
+//
+// A tile is 64 consecutive quads (256 elements) of a row, held by 4
+// consecutive threads with 16 float4 slots each: lane l of the tile holds quad
+// 4 j + l in slot j. Inside the tile the element index is 64 j_hi + 16 j_lo +
+// 4 l + c, so base-4 digit 0 is the float4 component c, digit 1 the lane l,
+// digit 2 the low two bits of j and digit 3 its high two bits. Digits below n
+// lie inside one group; the rest number the groups of the tile.
+//
+// Digits held in registers use the row structure of 2 H4: every row is all
+// ones except a -1 at the mirrored place, so along one digit
+// y_i = (x_0 + x_1 + x_2 + x_3) - 2 x_{3-i} (3 adds and 4 fmas, the output
+// staying at its own digit value; the signs D are part of the formula).
+// The lane digit is 2 H4 = D1 P W1 D1 applied by two shuffle butterflies.
+// Rather than flipping input signs, each lane keeps a value that is the true
+// one times a known sign and folds the partner's sign into the fma
+// coefficient; the last sign and D1 at the output go into the quantization
+// multiplier, and P (lanes 1 and 2 trade places) into the store address.
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ void h4_regs(float &a0, float &a1, float &a2, float &a3)
+{
+    const float s = (a0 + a1) + (a2 + a3);
+    const float y0 = fmaf(-2.0f, a3, s), y1 = fmaf(-2.0f, a2, s);
+    const float y2 = fmaf(-2.0f, a1, s), y3 = fmaf(-2.0f, a0, s);
+    a0 = y0;
+    a1 = y1;
+    a2 = y2;
+    a3 = y3;
+}
+
+// Per lane l of a tile: butterfly coefficients of the two shuffle levels, the
+// sign the kept value carries at the end (times D1 at the output), and P(l).
+__device__ __forceinline__ float lane_c0(int l) { return (l == 0 || l == 3) ? 1.0f : -1.0f; }
+__device__ __forceinline__ float lane_c1(int l) { return (l == 0 || l == 3) ? -1.0f : 1.0f; }
+__device__ __forceinline__ int lane_out(int l) { return ((l & 1) << 1) | (l >> 1); }
+
+__device__ __forceinline__ void h4_lanes(float &v, float c0, float c1)
+{
+    v = fmaf(c0, v, __shfl_xor_sync(kFull, v, 1));
+    v = fmaf(c1, v, __shfl_xor_sync(kFull, v, 2));
+}
+
+// Round half away from zero of the exact product v * inv: with h = +-1/2
+// carrying the product's sign, the fma rounded toward zero never crosses the
+// integer that truncation keeps, so trunc(fma_rz(v, inv, h)) is that integer.
+// `half_bits` is 1/2 with the sign of inv.
+__device__ __forceinline__ float code_of(float v, float inv, uint32_t half_bits)
+{
+    const float h = __uint_as_float((__float_as_uint(v) & kSign) ^ half_bits);
+    return truncf(__fmaf_rz(v, inv, h));
+}
+
+// One thread's share of a tile: load, rotate, absmax, quantize and store.
+
+template <int N>
+__device__ __forceinline__ void rotate_g256(float4 (&v)[16], int l)
+{
+#pragma unroll
+    for (int j = 0; j < 16; ++j) h4_regs(v[j].x, v[j].y, v[j].z, v[j].w);  // digit 0
+    if constexpr (N >= 2) {                                                  // digit 1
+        const float c0 = lane_c0(l), c1 = lane_c1(l);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            h4_lanes(v[j].x, c0, c1);
+            h4_lanes(v[j].y, c0, c1);
+            h4_lanes(v[j].z, c0, c1);
+            h4_lanes(v[j].w, c0, c1);
+        }
+    }
+    if constexpr (N >= 3) {  // digit 2: slots 4 b + (0..3)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            float4 &p0 = v[4 * b], &p1 = v[4 * b + 1], &p2 = v[4 * b + 2], &p3 = v[4 * b + 3];
+            h4_regs(p0.x, p1.x, p2.x, p3.x);
+            h4_regs(p0.y, p1.y, p2.y, p3.y);
+            h4_regs(p0.z, p1.z, p2.z, p3.z);
+            h4_regs(p0.w, p1.w, p2.w, p3.w);
+        }
+    }
+    if constexpr (N >= 4) {  // digit 3: slots b + 4 (0..3)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            float4 &p0 = v[b], &p1 = v[b + 4], &p2 = v[b + 8], &p3 = v[b + 12];
+            h4_regs(p0.x, p1.x, p2.x, p3.x);
+            h4_regs(p0.y, p1.y, p2.y, p3.y);
+            h4_regs(p0.z, p1.z, p2.z, p3.z);
+            h4_regs(p0.w, p1.w, p2.w, p3.w);
+        }
+    }
+}
+
+__device__ __forceinline__ float absmax_g256(const float4 (&v)[16])
+{
+    float m = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+        m = fmaxf(m, fmaxf(fmaxf(fabsf(v[j].x), fabsf(v[j].y)), fmaxf(fabsf(v[j].z), fabsf(v[j].w))));
+    return m;
+}
+
+// Codes of slots j < nv. q0 is the thread's slot-0 quad (tile * 64 + l); inv the
+// multiplier from scale_of.
+template <int N, bool kBf16>
+__device__ __forceinline__ void store_g256(const float4 (&v)[16], int nv, int l, int q0, char *qrow, float inv)
+{
+    if constexpr (N >= 2) inv *= lane_c1(l);  // the kept value's sign times D1 at the output
+    const uint32_t half_bits = 0x3f000000u | (__float_as_uint(inv) & kSign);
+    const int qo = q0 - l + (N >= 2 ? lane_out(l) : l);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        if (j >= nv) break;
+        const float r0 = code_of(v[j].x, inv, half_bits), r1 = code_of(v[j].y, inv, half_bits);
+        const float r2 = code_of(v[j].z, inv, half_bits), r3 = code_of(v[j].w, inv, half_bits);
+        if constexpr (kBf16) {
+            // |r| <= 127: the bf16 of r is the top half of its fp32 bits (a zero code may be -0)
+            const uint32_t lo = __byte_perm(__float_as_uint(r0), __float_as_uint(r1), 0x7632);
+            const uint32_t hi = __byte_perm(__float_as_uint(r2), __float_as_uint(r3), 0x7632);
+            reinterpret_cast<uint2 *>(qrow)[qo + 4 * j] = make_uint2(lo, hi);
+        } else {
+            // r + 1.5 * 2^23 holds r in its low mantissa bits: the low byte is r as int8
+            constexpr float kMagic = 12582912.0f;
+            const uint32_t w0 = __float_as_uint(r0 + kMagic), w1 = __float_as_uint(r1 + kMagic);
+            const uint32_t w2 = __float_as_uint(r2 + kMagic), w3 = __float_as_uint(r3 + kMagic);
+            reinterpret_cast<uint32_t *>(qrow)[qo + 4 * j] =
+                __byte_perm(__byte_perm(w0, w1, 0x0040), __byte_perm(w2, w3, 0x0040), 0x5410);
+        }
+    }
+}
+
+// Slots holding data: quad q0 + 4 j < kq. Whole groups are in or out.
+__device__ __forceinline__ int valid_slots(int kq, int q0)
+{
+    const int nv = (kq - q0 + 3) >> 2;
+    return nv < 0 ? 0 : (nv > 16 ? 16 : nv);
+}
+
+// Row-wide maximum of m over the tpr threads of each row of the CTA: segment
+// shuffles, then the segments' partial maxima through shared memory. The
+// caller synchronizes between writing `part` and calling row_max_read.
+__device__ __forceinline__ void row_max_write(float m, int tpr, float *part)
+{
+    const int seg = (tpr & 31) == 0 ? 32 : (tpr & -tpr);
+    for (int off = seg >> 1; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, off));
+    if (((threadIdx.x & 31) & (seg - 1)) == 0) part[threadIdx.x / seg] = m;
+}
+
+__device__ __forceinline__ float row_max_read(int tpr, int r_local, const float *part)
+{
+    const int seg = (tpr & 31) == 0 ? 32 : (tpr & -tpr);
+    const int p0 = (r_local * tpr) / seg, np = tpr / seg;
+    float amax = 0.0f;
+    for (int i = 0; i < np; ++i) amax = fmaxf(amax, part[p0 + i]);
+    return amax;
+}
+
+// Direct form: registers loaded straight from global memory, one pass per CTA;
+// rows longer than one CTA holds are split over a cluster.
+template <int N, bool kBf16>
+__global__ void __launch_bounds__(512) pack_g256_kernel(PackArgs a, DirectPlan L, int64_t row0)
+{
+    const int cl = L.cl;
+    const int cr = cl > 1 ? static_cast<int>(blockIdx.x % cl) : 0;
+    const int64_t cta_block = cl > 1 ? blockIdx.x / cl : blockIdx.x;
+    const int tpr = L.threads_per_row;
+    const int r_local = threadIdx.x / tpr;
+    const int t_cta = threadIdx.x - r_local * tpr;
+    const int64_t row = row0 + cta_block * L.rows_per_cta + r_local;
+    const bool row_ok = row < a.rows;
+    const int t_row = cr * tpr + t_cta;
+    const int kq = a.k >> 2, kpq = a.kpad >> 2;
+    const int l = t_row & 3;
+    const int q0 = (t_row >> 2) * 64 + l;
+    const int nv = row_ok ? valid_slots(kq, q0) : 0;
+
+    const float4 *src = reinterpret_cast<const float4 *>(a.x + (row_ok ? row : 0) * a.ldx) + q0;
+    float4 v[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) v[j] = j < nv ? __ldcs(src + 4 * j) : make_float4(0.f, 0.f, 0.f, 0.f);
+    rotate_g256<N>(v, l);
+
+    __shared__ float part[128];
+    __shared__ float cta_max;
+    row_max_write(absmax_g256(v), tpr, part);
+    __syncthreads();
+    float amax = row_max_read(tpr, r_local, part);
+    if (cl > 1) {
+        if (threadIdx.x == 0) cta_max = amax;
+        cluster_sync_all();  // every CTA's cta_max is written
+        amax = 0.0f;
+        for (int r = 0; r < cl; ++r) amax = fmaxf(amax, ld_cluster_f32(cluster_smem_addr(&cta_max, r)));
+    }
+    float inv;
+    const float s = scale_of(amax, N, &inv);
+    if (row_ok) {
+        if (t_row == 0) a.scale[row] = s;
+        char *qrow = static_cast<char *>(a.q) + row * a.ldq * (kBf16 ? 2 : 1);
+        store_g256<N, kBf16>(v, nv, l, q0, qrow, inv);
+        zero_pad<kBf16>(qrow, kq, kpq, t_row, tpr * cl);
+    }
+    if (cl > 1) cluster_sync_all();  // no CTA leaves while another may still read its cta_max
+}
+
+// Ring form: persistent CTAs, several per SM, each streaming blocks of whole
+// rows into its own shared-memory ring by bulk copies (cp.async.bulk, one per
+// row, completion counted in bytes on the stage's mbarrier), stages - 1
+// blocks ahead of the arithmetic. CTAs on one SM drift out of phase, so the
+// copies of some overlap the arithmetic and stores of others.
+constexpr int kMaxStages = 8;
+
+struct RingPlan {
+    int threads_per_row;  // 4 per 256-element tile
+    int rows_per_stage;
+    int stages;
+    uint32_t row_bytes;    // k * 4
+    uint32_t stage_bytes;  // rows_per_stage * row_bytes
+};
+
+__device__ __forceinline__ uint64_t globaltimer()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+constexpr uint64_t kTimeoutNs = 4000000000ull;  // 4 s
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    for (;;) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer() - t0 > kTimeoutNs) return false;
+    }
+}
+
+template <int N, bool kBf16>
+__global__ void __launch_bounds__(512) pack_ring_kernel(PackArgs a, RingPlan P)
+{
+    extern __shared__ __align__(128) uint8_t ring[];
+    __shared__ __align__(8) uint64_t full_bar[kMaxStages];
+    __shared__ float part[2][128];
+
+    const int tpr = P.threads_per_row, R = P.rows_per_stage, NS = P.stages;
+    const int r_local = threadIdx.x / tpr;
+    const int t_row = threadIdx.x - r_local * tpr;
+    const int kq = a.k >> 2, kpq = a.kpad >> 2;
+    const int l = t_row & 3;
+    const int q0 = (t_row >> 2) * 64 + l;
+    const int nv = valid_slots(kq, q0);
+    const int64_t nblocks = (a.rows + R - 1) / R;
+    const uint32_t ring_base = static_cast<uint32_t>(__cvta_generic_to_shared(ring));
+    const uint32_t bar_base = static_cast<uint32_t>(__cvta_generic_to_shared(full_bar));
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NS; ++s)
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar_base + 8u * s) : "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+
+    auto issue = [&](int stage, int64_t blk) {
+        if (blk >= nblocks) return;
+        const int64_t r0 = blk * R;
+        const int nr = a.rows - r0 < R ? static_cast<int>(a.rows - r0) : R;
+        const uint32_t bar = bar_base + 8u * stage;
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+                     "r"(static_cast<uint32_t>(nr) * P.row_bytes)
+                     : "memory");
+        for (int i = 0; i < nr; ++i)
+            asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                             ring_base + stage * P.stage_bytes + i * P.row_bytes),
+                         "l"(a.x + (r0 + i) * a.ldx), "r"(P.row_bytes), "r"(bar)
+                         : "memory");
+    };
+
+    if (threadIdx.x == 0)
+        for (int s = 0; s < NS - 1; ++s) issue(s, blockIdx.x + static_cast<int64_t>(s) * gridDim.x);
+
+    int it = 0;
+    bool ok = true;
+    for (int64_t blk = blockIdx.x; blk < nblocks; blk += gridDim.x, ++it) {
+        const int stage = it % NS;
+        if (threadIdx.x == 0) {
+            // the stage refilled here was read into registers before the previous barrier
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            issue((it + NS - 1) % NS, blk + static_cast<int64_t>(NS - 1) * gridDim.x);
+        }
+        const bool got = mbar_wait(bar_base + 8u * stage, static_cast<uint32_t>(it / NS) & 1u);
+        const int64_t row = blk * R + r_local;
+        const bool row_ok = got && row < a.rows;
+        const float4 *src = reinterpret_cast<const float4 *>(ring + stage * P.stage_bytes + r_local * P.row_bytes) + q0;
+        float4 v[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] = (row_ok && j < nv) ? src[4 * j] : make_float4(0.f, 0.f, 0.f, 0.f);
+        rotate_g256<N>(v, l);
+        float *pp = part[it & 1];
+        row_max_write(absmax_g256(v), tpr, pp);
+        // every thread agrees on whether the stage arrived; a failed wait ends the loop everywhere
+        if (!__syncthreads_and(got)) {
+            ok = false;
+            break;
+        }
+        float inv;
+        const float s = scale_of(row_max_read(tpr, r_local, pp), N, &inv);
+        if (row < a.rows) {
+            if (t_row == 0) a.scale[row] = s;
+            char *qrow = static_cast<char *>(a.q) + row * a.ldq * (kBf16 ? 2 : 1);
+            store_g256<N, kBf16>(v, nv, l, q0, qrow, inv);
+            zero_pad<kBf16>(qrow, kq, kpq, t_row, tpr);
+        }
+    }
+    if (!ok && threadIdx.x == 0) {
+        if (a.dev_status) atomicExch(a.dev_status, static_cast<int32_t>(CONVROT_ERR_TIMEOUT));
+        // let the copies already issued land before the CTA's shared memory goes away
+        int64_t blk = blockIdx.x + static_cast<int64_t>(it) * gridDim.x;
+        for (int s = 0; s < NS; ++s, blk += gridDim.x)
+            if (blk < nblocks) mbar_wait(bar_base + 8u * ((it + s) % NS), static_cast<uint32_t>((it + s) / NS) & 1u);
+    }
+}
+
 struct Shape {
     int lanes, S;
 };
-
-Shape shape_for(int log4g)
-{
-    if (log4g <= 4) return {3, 8};   // G <= 256
-    if (log4g == 5) return {5, 8};   // G = 1024
-    return {5, 32};                  // G = 4096
-}
 
 int gcd_int(int x, int y)
 {
@@ -354,10 +686,9 @@ DirectPlan direct_plan(const Shape &sh, int k)
     return L;
 }
 
-template <int LANES, int S, bool kBf16>
-cudaError_t launch_shape(const PackArgs &a, cudaStream_t stream)
+template <typename Kernel>
+cudaError_t launch_plan(Kernel kern, const Shape sh, const PackArgs &a, cudaStream_t stream)
 {
-    const Shape sh{LANES, S};
     const DirectPlan L = direct_plan(sh, a.k);
     if (L.cl > 16) return cudaErrorInvalidConfiguration;
     const int64_t row_blocks = (a.rows + L.rows_per_cta - 1) / L.rows_per_cta;
@@ -376,7 +707,6 @@ cudaError_t launch_shape(const PackArgs &a, cudaStream_t stream)
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        auto kern = pack_kernel<LANES, S, kBf16>;
         if (L.cl > 8) {
             cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
             if (e != cudaSuccess) return e;
@@ -388,13 +718,81 @@ cudaError_t launch_shape(const PackArgs &a, cudaStream_t stream)
 }
 
 
+// Ring form tuning: CTAs per SM, ring bytes per CTA, and CTA size to aim for.
+constexpr int kRingCtasPerSm = 2;
+constexpr uint32_t kRingBytes = 100 * 1024;
+constexpr uint32_t kRingBytesSolo = 200 * 1024;  // one CTA per SM, for long rows
+constexpr int kRingThreadsTarget = 128;
+
+struct RingLaunch {
+    RingPlan P;
+    int ctas_per_sm;  // 0: rows too long for a ring
+};
+
+RingLaunch ring_plan(int k)
+{
+    RingLaunch L{};
+    const int T = threads_per_row(Shape{2, 16}, k);
+    const int step = 32 / gcd_int(T, 32);  // rows per stage must fill whole warps
+    const uint64_t row_bytes = 4ull * static_cast<uint64_t>(k);
+    if (step * T > 512) return L;
+    int R = step;
+    while (R * T < kRingThreadsTarget && (R + step) * T <= 512) R += step;
+    uint32_t budget = kRingBytes;
+    L.ctas_per_sm = kRingCtasPerSm;
+    while (R > step && 2ull * R * row_bytes > budget) R -= step;
+    if (2ull * R * row_bytes > budget) {
+        budget = kRingBytesSolo;
+        L.ctas_per_sm = 1;
+        if (2ull * R * row_bytes > budget) return RingLaunch{};
+    }
+    L.P.threads_per_row = T;
+    L.P.rows_per_stage = R;
+    L.P.row_bytes = static_cast<uint32_t>(row_bytes);
+    L.P.stage_bytes = static_cast<uint32_t>(R * row_bytes);
+    const int ns = static_cast<int>(budget / L.P.stage_bytes);
+    L.P.stages = ns > kMaxStages ? kMaxStages : ns;
+    return L;
+}
+
+template <typename Kernel>
+cudaError_t launch_ring(Kernel kern, const RingLaunch &L, const PackArgs &a, cudaStream_t stream)
+{
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const int smem = L.P.stages * static_cast<int>(L.P.stage_bytes);
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    const int64_t nblocks = (a.rows + L.P.rows_per_stage - 1) / L.P.rows_per_stage;
+    const int64_t slots = static_cast<int64_t>(sms) * L.ctas_per_sm;
+    const int64_t grid = nblocks < slots ? nblocks : slots;
+    kern<<<static_cast<unsigned>(grid), L.P.threads_per_row * L.P.rows_per_stage, smem, stream>>>(a, L.P);
+    return cudaGetLastError();
+}
+
+template <int N, bool kBf16>
+cudaError_t launch_g256(const PackArgs &a, cudaStream_t stream)
+{
+    const RingLaunch L = ring_plan(a.k);
+    if (L.ctas_per_sm > 0) return launch_ring(pack_ring_kernel<N, kBf16>, L, a, stream);
+    return launch_plan(pack_g256_kernel<N, kBf16>, Shape{2, 16}, a, stream);
+}
+
 template <bool kBf16>
 cudaError_t dispatch(const PackArgs &a, cudaStream_t stream)
 {
-    if (a.log4g <= 4) return launch_shape<3, 8, kBf16>(a, stream);   // G <= 256
-    if (a.log4g == 5) return launch_shape<5, 8, kBf16>(a, stream);   // G = 1024
-    if (a.log4g == 6) return launch_shape<5, 32, kBf16>(a, stream);  // G = 4096
-    return cudaErrorInvalidValue;
+    switch (a.log4g) {
+    case 1: return launch_g256<1, kBf16>(a, stream);
+    case 2: return launch_g256<2, kBf16>(a, stream);
+    case 3: return launch_g256<3, kBf16>(a, stream);
+    case 4: return launch_g256<4, kBf16>(a, stream);
+    case 5: return launch_plan(pack_kernel<5, 8, kBf16>, Shape{5, 8}, a, stream);    // G = 1024
+    case 6: return launch_plan(pack_kernel<5, 32, kBf16>, Shape{5, 32}, a, stream);  // G = 4096
+    default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace

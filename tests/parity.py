@@ -10,7 +10,10 @@ Safetensors", stable-diffusion.cpp docs):
     fp64, so values that close to a boundary may round either way);
   - given identical codes: the int32 accumulators are bit-exact, and
     |Y - Y_ref| <= 1e-6 * (|A s_x s_w| + |b|) elementwise (Y_ref in fp64);
-  - end to end from X: max |Y - Y_ref| <= 1e-3 * max |Y_ref|.
+  - end to end from X: |Y - Y_ref| <= 1e-3 * max |Y_ref|
+    + 127 * s_x[r] s_w[o] * (flips_x[r] + flips_w[o]), where flips counts the
+    codes of row r of X (row o of W) that the previous rule let differ: each
+    such code moves the integer product by at most 127, times the scales.
 """
 
 from __future__ import annotations
@@ -61,7 +64,16 @@ def check_y_same_codes(y_gpu: np.ndarray, y64_ref: np.ndarray, A: np.ndarray, sx
     assert not bad.any(), f"{bad.sum()} outputs off; worst {np.max(err / np.maximum(base, 1e-300)):.3e}"
 
 
-def check_y_end_to_end(y_gpu: np.ndarray, y_ref: np.ndarray):
-    err = np.max(np.abs(np.asarray(y_gpu, np.float64) - np.asarray(y_ref, np.float64)))
+def check_y_end_to_end(y_gpu: np.ndarray, y_ref: np.ndarray, qx=None, qw=None, sx=None, sw=None):
+    """qx = (gpu codes, oracle codes) of the rows of X behind y, qw likewise for W,
+    sx, sw the GPU's scales; without them no code may have flipped."""
+    err = np.abs(np.asarray(y_gpu, np.float64) - np.asarray(y_ref, np.float64))
     ref = np.max(np.abs(np.asarray(y_ref, np.float64)))
-    assert err <= Y_END_TO_END * ref, f"max|dY| = {err:.3e} > 1e-3 * {ref:.3e}"
+    tol = np.full(err.shape, Y_END_TO_END * ref)
+    if qx is not None:
+        fx = (np.asarray(qx[0], np.int32) != np.asarray(qx[1], np.int32)).sum(axis=1).astype(np.float64)
+        fw = (np.asarray(qw[0], np.int32) != np.asarray(qw[1], np.int32)).sum(axis=1).astype(np.float64)
+        tol = tol + 127.0 * (1 + 1e-6) * (np.asarray(sx, np.float64)[:, None] * np.asarray(sw, np.float64)[None, :]
+                                          * (fx[:, None] + fw[None, :]))
+    bad = err > tol
+    assert not bad.any(), f"{bad.sum()} outputs off end to end; worst |dY| = {err.max():.3e}, 1e-3 * max|Y| = {Y_END_TO_END * ref:.3e}"

@@ -99,6 +99,20 @@ def test_pack_matches_oracle(G, k, codes):
     assert float(p.scale[0]) == 0.0 and torch.all(p.q[0, :cr.convrot_ldq(k)] == 0)
 
 
+@pytest.mark.parametrize("G,k,m", [(256, 768, 3000), (4, 768, 3000), (64, 16384, 700), (256, 28672, 40)],
+                         ids=["ring-wraps", "ring-wraps-G4", "ring-one-cta-per-sm", "direct"])
+@pytest.mark.parametrize("codes", CODES, ids=CODE_IDS)
+def test_pack_launch_forms(G, k, m, codes):
+    """Each launch form of the G <= 256 pack: a shared-memory ring that wraps many
+    times, a ring of one CTA per SM (long rows), and the direct form."""
+    rng = np.random.default_rng(G + k + m)
+    X = special_rows(rng, m, k)
+    p = gpu_pack(X, G, codes)
+    Q, s, v = oracle.pack_rows(X, G)
+    parity.check_scales(p.scale.cpu().numpy(), s)
+    parity.check_codes(codes_np(p), Q, v)
+
+
 def test_pack_hand_worked_rows(golden_dir):
     cases = json.load(open(os.path.join(golden_dir, "hand_worked_rows.json")))["rows"]
     for c in cases:
@@ -209,7 +223,8 @@ def test_linear_end_to_end_tiny(codes):
     parity.check_codes(codes_np(px), ref["Qx"], ref["vx"])
     Qw_ref, _, vw = oracle.pack_rows(W, wl.G)
     parity.check_codes(codes_np(pw), Qw_ref, vw)
-    parity.check_y_end_to_end(Y.cpu().numpy(), ref["Y64"])
+    parity.check_y_end_to_end(Y.cpu().numpy(), ref["Y64"], (codes_np(px), ref["Qx"]), (codes_np(pw), Qw_ref),
+                              px.scale.cpu().numpy(), pw.scale.cpu().numpy())
     # with the GPU's own codes the integer product and the epilogue are exact
     qx, qw = codes_np(px).astype(np.int8), codes_np(pw).astype(np.int8)
     A_ref = oracle.gemm_i32(qx, qw, wl.k)
@@ -258,7 +273,7 @@ def test_full_size_sampled(name):
     # end to end against the oracle's own codes
     A_ref = oracle.gemm_i32(Qx_ref, Qw_ref, wl.k)
     _, Y64_ref = oracle.reconstruct(A_ref, sx_ref, sw_ref, b)
-    parity.check_y_end_to_end(Y_rows, Y64_ref)
+    parity.check_y_end_to_end(Y_rows, Y64_ref, (qx_gpu, Qx_ref), (qw_gpu, Qw_ref), sx_gpu, sw_gpu)
 
 
 def test_grouped_linears_share_one_pack():
@@ -280,7 +295,9 @@ def test_grouped_linears_share_one_pack():
         assert torch.equal(view, single)
     # and against the oracle, end to end
     ref = oracle.linear(X, np.concatenate(Ws), np.concatenate(bs), 64)
-    parity.check_y_end_to_end(Y.cpu().numpy(), ref["Y64"])
+    Qw_ref, _, _ = oracle.pack_rows(np.concatenate(Ws), 64, want_pre_round=False)
+    parity.check_y_end_to_end(Y.cpu().numpy(), ref["Y64"], (codes_np(px), ref["Qx"]), (codes_np(pw), Qw_ref),
+                              px.scale.cpu().numpy(), pw.scale.cpu().numpy())
 
 
 @pytest.mark.slow
@@ -299,4 +316,5 @@ def test_full_size_attention_grouped_qkv():
     Qw_ref, sw_ref, _ = oracle.pack_rows(np.concatenate(Ws), wl.G, want_pre_round=False)
     A_ref = oracle.gemm_i32(Qx_ref, Qw_ref, wl.k)
     _, Y64 = oracle.reconstruct(A_ref, sx_ref, sw_ref, np.concatenate(bs))
-    parity.check_y_end_to_end(Y[torch.from_numpy(rows).cuda()].cpu().numpy(), Y64)
+    parity.check_y_end_to_end(Y[torch.from_numpy(rows).cuda()].cpu().numpy(), Y64, (codes_np(px)[rows], Qx_ref),
+                              (codes_np(pw), Qw_ref), px.scale.cpu().numpy()[rows], pw.scale.cpu().numpy())
