@@ -28,6 +28,8 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
+from int8_hadamard_rotated_convrot_gb300.inputs import stage_shapes  # noqa: E402  (seeded shapes only)
+
 METRIC = "convrot linear INT8 TOPS + pack GB/s at 4096x3072x12288, % of roofline"
 L2_BYTES = 129 * 1024 * 1024
 
@@ -146,14 +148,16 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- CPU baseline (the oracle)
-def oracle_sample_run(wl, rows: int, Qw, sw, X, b):
-    """One oracle pass over `rows` rows of the workload: pack, integer GEMM, reconstruct."""
+def oracle_sample_run(wl, rows: int, packed_w, X):
+    """One oracle pass over `rows` rows of the workload: for each stage pack,
+    integer GEMM and reconstruct (with the stage's activation)."""
     import oracle
 
-    Xs = X[:rows]
-    Qx, sx, _ = oracle.pack_rows(Xs, wl.G, want_pre_round=False)
-    A = oracle.gemm_i32(Qx, Qw, wl.k)
-    oracle.reconstruct(A, sx, sw, b)
+    H = X[:rows]
+    for (Qw, sw, b), st in zip(packed_w, stage_shapes(wl)):
+        Qx, sx, _ = oracle.pack_rows(H, wl.G, want_pre_round=False)
+        A = oracle.gemm_i32(Qx, Qw, st.k)
+        H, _ = oracle.reconstruct(A, sx, sw, b, st.act)
 
 
 def cpu_baseline(wl, budget_s: float, steps: int = 1, warmup: int = 0):
@@ -163,28 +167,39 @@ def cpu_baseline(wl, budget_s: float, steps: int = 1, warmup: int = 0):
 
     oracle.build()
     X = inputs.activations(wl)
-    W, b = inputs.weights(wl), inputs.bias(wl)
-    Qw, sw, _ = oracle.pack_rows(W, wl.G, want_pre_round=False)  # offline, untimed
+    packed_w = []
+    for s_i, _ in enumerate(stage_shapes(wl)):  # offline, untimed
+        Ws, b = inputs.stage_weights(wl, s_i)
+        Qw, sw, _ = oracle.pack_rows(np.concatenate(Ws), wl.G, want_pre_round=False)
+        packed_w.append((Qw, sw, b))
     per_row, trial = 1.0, 2
     for _ in range(2):  # calibrate on a small, then a larger trial
         t0 = time.perf_counter()
-        oracle_sample_run(wl, trial, Qw, sw, X, b)
+        oracle_sample_run(wl, trial, packed_w, X)
         per_row = max((time.perf_counter() - t0) / trial, 1e-6)
         trial = int(max(2, min(X.shape[0], 0.2 * budget_s / max(steps, 1) / per_row)))
     rows = int(max(2, min(X.shape[0], budget_s / max(steps, 1) / per_row)))
     for _ in range(warmup):
-        oracle_sample_run(wl, rows, Qw, sw, X, b)
+        oracle_sample_run(wl, rows, packed_w, X)
     times = []
     for _ in range(steps):
         t0 = time.perf_counter()
-        oracle_sample_run(wl, rows, Qw, sw, X, b)
+        oracle_sample_run(wl, rows, packed_w, X)
         times.append(time.perf_counter() - t0)
     t = sum(times) / len(times)
-    ops = 2.0 * rows * wl.n * wl.k
+    ops = wl.step_ops * rows / wl.m
+    what = " then ".join(f"pack + int GEMM vs {st.n} weight rows + reconstruct" for st in stage_shapes(wl))
     return {"value": ops / t / 1e12, "unit": "TOPS", "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": f"{rows} of {wl.m} rows of {wl.name} (pack + int GEMM vs all {wl.n} weight rows "
-                      f"+ reconstruct), fp64 oracle, {len(times)} step(s) of {t:.2f} s",
+            "sample": f"{rows} of {wl.m} rows of {wl.name} ({what}), fp64 oracle, "
+                      f"{len(times)} step(s) of {t:.2f} s",
             "seconds_per_step": t}
+
+
+def workload_name(wl) -> str:
+    if wl.down_n:
+        return f"{wl.name} M{wl.m} K{wl.k} N{wl.n} (GELU in the epilogue) -> K{wl.n} N{wl.down_n} G{wl.G}"
+    grouped = f"x{wl.linears} (one grouped GEMM)" if wl.linears > 1 else ""
+    return f"{wl.name} M{wl.m} K{wl.k} N{wl.n}{grouped} G{wl.G}"
 
 
 def run_reference(args):
@@ -201,8 +216,7 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": cb["seconds_per_step"] * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": f"{wl.name} M{wl.m} K{wl.k} N{wl.n} G{wl.G}",
-                   "sample": cb["sample"]},
+        "config": {"workload": workload_name(wl), "sample": cb["sample"]},
         "cpu_baseline": {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")},
         "e2e": {"value": cb["value"], "unit": "TOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -234,31 +248,42 @@ def run_ours(args):
     codes = {"i8": cr.CODES_I8, "bf16": cr.CODES_BF16, "auto": cr.CODES_BF16}[args.codes]
 
     # inputs: every rank runs the full workload on its own GPU (weak scaling; rows are independent)
+    stages = stage_shapes(wl)
     X = torch.from_numpy(inputs.activations(wl)).to(dev)
-    # linears sharing the packed input (q, k, v) run as one grouped GEMM over concatenated weights
-    Ws = [torch.from_numpy(inputs.weights(wl, i)).to(dev) for i in range(wl.linears)]
-    b = torch.from_numpy(np.concatenate([inputs.bias(wl, i) for i in range(wl.linears)])).to(dev)
-    n_all = wl.n * wl.linears
-    touched = wl.m * wl.k * 4 + n_all * wl.k * (1 if codes == cr.CODES_I8 else 2) + wl.m * n_all * 4
+    code_b = 1 if codes == cr.CODES_I8 else 2
+    touched = wl.m * wl.k * 4 + sum(st.n * st.k * code_b + wl.m * st.n * 4 + wl.m * st.k * code_b for st in stages)
     R = max(2, -(-3 * L2_BYTES // touched) + 1)  # rotating sets so a reuse is > 2 L2s away
     R = min(R, 6)
     Xs = [X] + [X.clone() for _ in range(R - 1)]
-    pws = [cr.quantize_weights_grouped(Ws, wl.G, codes) for _ in range(R)]
-    pxs = [cr.empty_packed(wl.m, wl.k, codes, dev) for _ in range(R)]
-    Ys = [torch.empty((wl.m, n_all), dtype=torch.float32, device=dev) for _ in range(R)]
-    del Ws
+    pws, biases, pxs, Ys = [], [], [], []
+    for s_i, st in enumerate(stages):
+        # linears sharing the packed input (q, k, v) run as one grouped GEMM over concatenated weights
+        Ws_np, b_np = inputs.stage_weights(wl, s_i)
+        Ws = [torch.from_numpy(W).to(dev) for W in Ws_np]
+        pws.append([cr.quantize_weights_grouped(Ws, wl.G, codes) for _ in range(R)])
+        biases.append(torch.from_numpy(b_np).to(dev))
+        pxs.append([cr.empty_packed(wl.m, st.k, codes, dev) for _ in range(R)])
+        Ys.append([torch.empty((wl.m, st.n), dtype=torch.float32, device=dev) for _ in range(R)])
+        del Ws
+    n_out = stages[-1].n
     stream = torch.cuda.current_stream(dev)
 
+    def run_stages(x_in, j, ev=None):
+        h = x_in
+        for s_i, st in enumerate(stages):
+            if ev is not None:
+                ev[2 * s_i].record(stream)
+            cr.convrot_pack_activations(h, wl.G, codes, out=pxs[s_i][j], stream=stream)
+            if ev is not None:
+                ev[2 * s_i + 1].record(stream)
+            cr.convrot_linear_act(pxs[s_i][j], pws[s_i][j], biases[s_i], st.act, out=Ys[s_i][j], stream=stream)
+            h = Ys[s_i][j]
+        if ev is not None:
+            ev[2 * len(stages)].record(stream)
+        return h
+
     def step(i, ev=None):
-        j = i % R
-        if ev is not None:
-            ev[0].record(stream)
-        cr.convrot_pack_activations(Xs[j], wl.G, codes, out=pxs[j], stream=stream)
-        if ev is not None:
-            ev[1].record(stream)
-        cr.convrot_linear(pxs[j], pws[j], b, out=Ys[j], stream=stream)
-        if ev is not None:
-            ev[2].record(stream)
+        run_stages(Xs[i % R], i % R, ev)
 
     for i in range(args.warmup):
         step(i)
@@ -276,7 +301,7 @@ def run_ours(args):
     clocks = ClockSampler(uuid)
     clocks.start()
     time.sleep(0.3)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * len(stages) + 1)] for _ in range(args.steps)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     # the timed loop runs several times over so the clock sampler sees a loaded GPU
@@ -289,8 +314,8 @@ def run_ours(args):
         pg.barrier()
     torch.cuda.synchronize(dev)
     total_ms = t_start.elapsed_time(t_end)
-    pack_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    gemm_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    pack_ms = [sum(e[2 * k].elapsed_time(e[2 * k + 1]) for k in range(len(stages))) for e in evs]
+    gemm_ms = [sum(e[2 * k + 1].elapsed_time(e[2 * k + 2]) for k in range(len(stages))) for e in evs]
     # keep the GPU busy a little longer with the same steps for the clock record
     t_keep = time.time()
     i = 0
@@ -303,14 +328,12 @@ def run_ours(args):
     # end to end through the public API: pinned host X in, pinned host Y out, every step
     e2e_steps = max(3, min(args.steps, 10))
     Xh = torch.from_numpy(inputs.activations(wl)).pin_memory()
-    Yh = torch.empty((wl.m, n_all), dtype=torch.float32).pin_memory()
+    Yh = torch.empty((wl.m, n_out), dtype=torch.float32).pin_memory()
     Xd = torch.empty_like(Xs[0])
 
     def e2e_step():
         Xd.copy_(Xh, non_blocking=True)
-        cr.convrot_pack_activations(Xd, wl.G, codes, out=pxs[0], stream=stream)
-        cr.convrot_linear(pxs[0], pws[0], b, out=Ys[0], stream=stream)
-        Yh.copy_(Ys[0], non_blocking=True)
+        Yh.copy_(run_stages(Xd, 0), non_blocking=True)
 
     for _ in range(2):
         e2e_step()
@@ -326,13 +349,13 @@ def run_ours(args):
 
     ms_step, e2e_ms = slowest_rank([total_ms / args.steps, e2e_ms], pg, dev)
 
-    ops = float(wl.int_ops) * wl.linears
+    ops = float(wl.step_ops)
     value = job_tops(world, ops, ms_step)
     gemm_avg = sum(gemm_ms) / len(gemm_ms)
     pack_avg = sum(pack_ms) / len(pack_ms)
     pk = peaks()
     gemm_tops = ops / (gemm_avg * 1e-3) / 1e12
-    pack_bytes = wl.m * (4 * wl.k + (1 if codes == cr.CODES_I8 else 2) * wl.k + 4)
+    pack_bytes = sum(wl.m * (4 * st.k + code_b * st.k + 4) for st in stages)
     pack_gbs = pack_bytes / (pack_avg * 1e-3) / 1e9
     traffic = measured_traffic(wl.name, "i8" if codes == cr.CODES_I8 else "bf16")
 
@@ -343,8 +366,7 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "s8" if codes == cr.CODES_I8 else "bf16-coded s8",
         "data": "synthetic (seeded N(0,1) activations with 0.1% outlier channels x50, N(0,0.02^2) weights)",
-        "config": {"workload": f"{wl.name} M{wl.m} K{wl.k} N{wl.n}" + (f"x{wl.linears} (one grouped GEMM)" if wl.linears > 1 else "")
-                   + f" G{wl.G}", "global_batch": wl.m * world,
+        "config": {"workload": workload_name(wl), "global_batch": wl.m * world,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "codes": "i8" if codes == cr.CODES_I8 else "bf16",
                    "l2": f"{R} rotating input/output sets, {touched / 1e6:.0f} MB touched per step (> L2)"},
@@ -356,9 +378,9 @@ def run_ours(args):
                           "frac": pack_gbs / pk["hbm_gbs"], "bytes_per_launch": pack_bytes,
                           "peak_source": f"{pk['source']} copy bandwidth"},
         "e2e": {"value": job_tops(world, ops, e2e_ms), "unit": "TOPS",
-                "h2d_bytes_per_step": wl.m * wl.k * 4, "d2h_bytes_per_step": wl.m * n_all * 4,
+                "h2d_bytes_per_step": wl.m * wl.k * 4, "d2h_bytes_per_step": wl.m * n_out * 4,
                 "ms_per_step": e2e_ms},
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": 2 * len(stages) * args.steps,
         "clocks": clk,
     }
     if not args.no_cpu_baseline and world == 1:

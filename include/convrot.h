@@ -67,6 +67,20 @@ typedef enum {
 } convrot_codes;
 
 /*
+ * Activation applied to Y inside the linear's epilogue. The page's layer is a
+ * plain linear; a DiT MLP applies GELU to its up projection's output before
+ * the down projection packs it, and fusing it here saves a separate pass over
+ * that output. GELU(v) = v * Phi(v) with Phi the standard normal CDF:
+ *   CONVROT_ACT_GELU_ERF   0.5 v (1 + erf(v / sqrt(2)))
+ *   CONVROT_ACT_GELU_TANH  0.5 v (1 + tanh(sqrt(2/pi) (v + 0.044715 v^3)))
+ */
+typedef enum {
+    CONVROT_ACT_NONE = 0,
+    CONVROT_ACT_GELU_ERF = 1,
+    CONVROT_ACT_GELU_TANH = 2
+} convrot_activation;
+
+/*
  * A packed, rotated and quantized row block: the page's "packed runtime
  * activation tensor" (I8 rows plus one floating-point scale per row,
  * "Runtime activation quantization"), and equally a quantized weight (Q_w,
@@ -144,6 +158,17 @@ convrot_status convrot_pack_activations(const float *X, int64_t m, int64_t k, in
  */
 convrot_status convrot_linear(const convrot_packed *x, const convrot_packed *w, const float *bias,
                               float *Y, int64_t ldy, int32_t *dev_status, cudaStream_t stream);
+
+/*
+ * The linear followed by an activation in the same epilogue:
+ * Y[r, o] = act(A[r, o] * s_x[r] * s_w[o] + b[o]). No counterpart on the page
+ * (it defines the linear alone); see convrot_activation.
+ *   act  a convrot_activation value; anything else is CONVROT_ERR_INVALID_ARG.
+ * Everything else as for convrot_linear (which is act = CONVROT_ACT_NONE).
+ */
+convrot_status convrot_linear_act(const convrot_packed *x, const convrot_packed *w, const float *bias,
+                                  int32_t act, float *Y, int64_t ldy, int32_t *dev_status,
+                                  cudaStream_t stream);
 
 /*
  * The integer GEMM alone: A[r, o] = sum_i Q_x[r, i] * Q_w[o, i] as int32, for

@@ -27,6 +27,7 @@ EXPORTED = [
     "convrot_quantize_weights",
     "convrot_pack_activations",
     "convrot_linear",
+    "convrot_linear_act",
     "convrot_gemm_i32",
     "convrot_status_string",
 ]
@@ -78,6 +79,8 @@ def load() -> ctypes.CDLL:
         lib.convrot_pack_activations.restype = ctypes.c_int
         lib.convrot_linear.argtypes = [P, P, vp, vp, i64, vp, vp]
         lib.convrot_linear.restype = ctypes.c_int
+        lib.convrot_linear_act.argtypes = [P, P, vp, i32, vp, i64, vp, vp]
+        lib.convrot_linear_act.restype = ctypes.c_int
         lib.convrot_gemm_i32.argtypes = [P, P, vp, i64, vp, vp]
         lib.convrot_gemm_i32.restype = ctypes.c_int
         lib.convrot_status_string.argtypes = [ctypes.c_int]
@@ -191,6 +194,24 @@ def convrot_linear(x: Packed, w: Packed, bias: torch.Tensor | None = None, out: 
     _check(load().convrot_linear(ctypes.byref(xs), ctypes.byref(ws), _ptr(bias), _ptr(out),
                                  out.stride(0) if out.dim() == 2 else 0, _ptr(dev_status),
                                  _stream(stream)), "convrot_linear")
+    return out
+
+
+ACT_NONE, ACT_GELU_ERF, ACT_GELU_TANH = 0, 1, 2
+
+
+def convrot_linear_act(x: Packed, w: Packed, bias: torch.Tensor | None, act: int,
+                       out: torch.Tensor | None = None, dev_status: torch.Tensor | None = None,
+                       stream=None) -> torch.Tensor:
+    """Y [m, n] fp32 = act((Q_x Q_w^T) * s_x s_w + b), act one of ACT_*."""
+    if out is None:
+        out = _padded_out(x.rows, w.rows, torch.float32, x.q.device)
+    if bias is not None and (bias.dtype != torch.float32 or not bias.is_cuda):
+        raise TypeError("bias must be a float32 CUDA tensor")
+    xs, ws = x.struct(), w.struct()
+    _check(load().convrot_linear_act(ctypes.byref(xs), ctypes.byref(ws), _ptr(bias), int(act), _ptr(out),
+                                     out.stride(0) if out.dim() == 2 else 0, _ptr(dev_status),
+                                     _stream(stream)), "convrot_linear_act")
     return out
 
 

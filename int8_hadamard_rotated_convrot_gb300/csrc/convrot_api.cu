@@ -97,8 +97,9 @@ convrot_status check_pair(const convrot_packed *x, const convrot_packed *w)
 }
 
 convrot_status run_gemm(const convrot_packed *x, const convrot_packed *w, const float *bias, float *Y,
-                        int32_t *A, int64_t ld, int32_t *dev_status, cudaStream_t stream)
+                        int32_t *A, int64_t ld, int32_t act, int32_t *dev_status, cudaStream_t stream)
 {
+    if (act < CONVROT_ACT_NONE || act > CONVROT_ACT_GELU_TANH) return CONVROT_ERR_INVALID_ARG;
     convrot_status st = check_pair(x, w);
     if (st != CONVROT_OK) return st;
     const int64_t m = x->rows, n = w->rows;
@@ -127,6 +128,7 @@ convrot_status run_gemm(const convrot_packed *x, const convrot_packed *w, const 
     g.a = A;
     g.ldy = ld;
     g.dev_status = dev_status;
+    g.act = act;
     cudaError_t e = x->codes == CONVROT_CODES_I8 ? convrot::launch_gemm_imma(g, stream)
                                                  : convrot::launch_gemm_tc(g, stream);
     if (e == cudaErrorNotSupported) return CONVROT_ERR_UNSUPPORTED;
@@ -155,14 +157,21 @@ convrot_status convrot_linear(const convrot_packed *x, const convrot_packed *w, 
                               float *Y, int64_t ldy, int32_t *dev_status, cudaStream_t stream)
 {
     if (!Y && x && w && x->rows > 0 && w->rows > 0) return CONVROT_ERR_INVALID_ARG;
-    return run_gemm(x, w, bias, Y, nullptr, ldy, dev_status, stream);
+    return run_gemm(x, w, bias, Y, nullptr, ldy, CONVROT_ACT_NONE, dev_status, stream);
+}
+
+convrot_status convrot_linear_act(const convrot_packed *x, const convrot_packed *w, const float *bias, int32_t act,
+                                  float *Y, int64_t ldy, int32_t *dev_status, cudaStream_t stream)
+{
+    if (!Y && x && w && x->rows > 0 && w->rows > 0) return CONVROT_ERR_INVALID_ARG;
+    return run_gemm(x, w, bias, Y, nullptr, ldy, act, dev_status, stream);
 }
 
 convrot_status convrot_gemm_i32(const convrot_packed *x, const convrot_packed *w, int32_t *A,
                                 int64_t lda, int32_t *dev_status, cudaStream_t stream)
 {
     if (!A && x && w && x->rows > 0 && w->rows > 0) return CONVROT_ERR_INVALID_ARG;
-    return run_gemm(x, w, nullptr, nullptr, A, lda, dev_status, stream);
+    return run_gemm(x, w, nullptr, nullptr, A, lda, CONVROT_ACT_NONE, dev_status, stream);
 }
 
 const char *convrot_status_string(convrot_status s)

@@ -156,11 +156,11 @@ __global__ void __launch_bounds__(THREADS) gemm_imma_kernel(GemmArgs g)
                     }
                 } else {
                     const float b0 = g.bias ? g.bias[c] : 0.f;
-                    const float y0 = fmaf(static_cast<float>(a0) * sxr, g.sw[c], b0);
+                    const float y0 = apply_act(fmaf(static_cast<float>(a0) * sxr, g.sw[c], b0), g.act);
                     float *dst = g.y + r * g.ldy + c;
                     if (c + 1 < g.n) {
                         const float b1 = g.bias ? g.bias[c + 1] : 0.f;
-                        const float y1 = fmaf(static_cast<float>(a1) * sxr, g.sw[c + 1], b1);
+                        const float y1 = apply_act(fmaf(static_cast<float>(a1) * sxr, g.sw[c + 1], b1), g.act);
                         *reinterpret_cast<float2 *>(dst) = make_float2(y0, y1);
                     } else {
                         dst[0] = y0;

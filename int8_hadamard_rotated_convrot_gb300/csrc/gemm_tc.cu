@@ -172,6 +172,7 @@ struct TcParams {
     int32_t *a;
     int64_t ldy;
     int32_t *dev_status;
+    int32_t act;  // convrot_activation on Y
 };
 
 
@@ -183,7 +184,25 @@ struct TcParams {
 // writes whole lines and clips rows >= m. A box that would cross column n is
 // written directly with masked stores instead. A buffer is reused only after
 // the store issued from it two boxes earlier has read it.
-template <bool kRawInt32>
+// Activation over the warp's staged 32 x 32 box (lane i owns row i), in a
+// loop unrolled only twice so that the accumulators of the boxes still to
+// come stay in registers while it runs (fully unrolled, the GELU's
+// temporaries pushed all 128 of them to local memory).
+template <int kAct>
+__device__ __forceinline__ void act_box(uint32_t buf, int lane)
+{
+#pragma unroll 2
+    for (int c = 0; c < 8; ++c) {
+        const uint32_t addr = buf + lane * (OUT_BOX * 4) + ((c ^ (lane & 7)) << 4);
+        float4 v;
+        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
+        v = make_float4(apply_act_t<kAct>(v.x), apply_act_t<kAct>(v.y), apply_act_t<kAct>(v.z), apply_act_t<kAct>(v.w));
+        asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
+                     : "memory");
+    }
+}
+
+template <bool kRawInt32, int kAct>
 __device__ __forceinline__ void store_tile_rows(const TcParams &p, const CUtensorMap *tmY, uint32_t out_smem,
                                                 uint32_t &store_iter, int64_t row0, int64_t col0,
                                                 const int32_t (&acc)[128], int lane, int ncols = 128)
@@ -196,6 +215,39 @@ __device__ __forceinline__ void store_tile_rows(const TcParams &p, const CUtenso
         if (cc * 32 >= ncols) break;
         const int64_t x = col0 + cc * 32;
         if (x >= p.n) break;
+        if (kAct != 0 && x + 32 > p.n) {
+            // ragged last box with an activation: stage, activate, then masked stores from shared memory
+            const uint32_t buf = out_smem + (store_iter & 1u) * OUT_BUF_BYTES;
+            if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+            __syncwarp();
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int64_t col = x + c * 4 + e;
+                    const float swv = col < p.n ? __ldg(p.sw + col) : 0.0f;
+                    const float bv = (p.bias && col < p.n) ? __ldg(p.bias + col) : 0.0f;
+                    w[e] = __float_as_uint(fmaf(static_cast<float>(acc[cc * 32 + c * 4 + e]) * sxr, swv, bv));
+                }
+                const uint32_t addr = buf + lane * (OUT_BOX * 4) + ((c ^ (lane & 7)) << 4);
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[0]), "r"(w[1]), "r"(w[2]),
+                             "r"(w[3])
+                             : "memory");
+            }
+            act_box<kAct>(buf, lane);
+            if (row < p.m) {
+#pragma unroll 1
+                for (int j = 0; j < 32 && x + j < p.n; ++j) {
+                    const uint32_t addr = buf + lane * (OUT_BOX * 4) + ((((j >> 2) ^ (lane & 7)) << 4) | ((j & 3) << 2));
+                    float v;
+                    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+                    p.y[row * p.ldy + x + j] = v;
+                }
+            }
+            __syncwarp();
+            continue;
+        }
         if (x + 32 > p.n) {
             // ragged last box: masked stores straight from registers
             if (row < p.m) {
@@ -244,6 +296,7 @@ __device__ __forceinline__ void store_tile_rows(const TcParams &p, const CUtenso
                          "r"(w[3])
                          : "memory");
         }
+        if constexpr (kAct != 0) act_box<kAct>(buf, lane);
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
         if (lane == 0) {
@@ -265,7 +318,7 @@ __device__ __forceinline__ void drain_stores(int lane)
     __syncwarp();
 }
 
-template <bool kRawInt32>
+template <bool kRawInt32, int kAct>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmY, TcParams p)
@@ -439,7 +492,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (lane == 0) mbar_arrive(acce_bar(buf));
             }
             if (!ok) break;
-            store_tile_rows<kRawInt32>(p, &tmY, out_smem, store_iter, mt * BM + q * 32, nt * BN + h * 128, acc, lane);
+            store_tile_rows<kRawInt32, kAct>(p, &tmY, out_smem, store_iter, mt * BM + q * 32, nt * BN + h * 128, acc, lane);
         }
         drain_stores(lane);
         if (!ok) fail();
@@ -550,7 +603,7 @@ __device__ __forceinline__ void arrive_remote(uint32_t cluster_bar)
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
 }
 
-template <int BN, bool kRawInt32>
+template <int BN, bool kRawInt32, int kAct>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmY, TcParams p)
@@ -732,7 +785,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                 if (lane == 0) arrive_remote(map_to_rank(acce_bar(buf), 0));
             }
             if (!ok) break;
-            store_tile_rows<kRawInt32>(p, &tmY, out_smem, store_iter, mt * 2 * BMC + static_cast<int64_t>(rank) * BMC + q * 32,
+            store_tile_rows<kRawInt32, kAct>(p, &tmY, out_smem, store_iter, mt * 2 * BMC + static_cast<int64_t>(rank) * BMC + q * 32,
                                        nt * BNP + h * 128, acc, lane, h == 0 ? 128 : BNP - 128);
         }
         drain_stores(lane);
@@ -811,18 +864,16 @@ cudaError_t launch_pair(const GemmArgs &g, const TcParams &p, const CUtensorMap 
     const int64_t tiles = ((g.m + 2 * pair::BMC - 1) / (2 * pair::BMC)) * ((g.n + BN - 1) / BN);
     const int64_t pairs = tiles < sms / 2 ? tiles : sms / 2;
     const unsigned grid = static_cast<unsigned>(2 * pairs);
-    if (g.a) {
-        auto k = pair::gemm_tc_pair_kernel<BN, true>;
-        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    auto run = [&](auto kern) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
         if (e != cudaSuccess) return e;
-        k<<<grid, THREADS, C::SMEM_BYTES, stream>>>(pa, pb, ty, p);
-    } else {
-        auto k = pair::gemm_tc_pair_kernel<BN, false>;
-        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        k<<<grid, THREADS, C::SMEM_BYTES, stream>>>(pa, pb, ty, p);
-    }
-    return cudaGetLastError();
+        kern<<<grid, THREADS, C::SMEM_BYTES, stream>>>(pa, pb, ty, p);
+        return cudaGetLastError();
+    };
+    if (g.a) return run(pair::gemm_tc_pair_kernel<BN, true, 0>);
+    if (p.act == 1) return run(pair::gemm_tc_pair_kernel<BN, false, 1>);
+    if (p.act == 2) return run(pair::gemm_tc_pair_kernel<BN, false, 2>);
+    return run(pair::gemm_tc_pair_kernel<BN, false, 0>);
 }
 
 }  // namespace
@@ -847,6 +898,7 @@ cudaError_t launch_gemm_tc(const GemmArgs &g, cudaStream_t stream)
     p.a = g.a;
     p.ldy = g.ldy;
     p.dev_status = g.dev_status;
+    p.act = g.act;
     p.vec_cols = (reinterpret_cast<uintptr_t>(g.sw) % 16 == 0) && (reinterpret_cast<uintptr_t>(g.bias) % 16 == 0);
     const int sms = sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
@@ -858,18 +910,16 @@ cudaError_t launch_gemm_tc(const GemmArgs &g, cudaStream_t stream)
     }
     const int64_t tiles = ((g.m + BM - 1) / BM) * ((g.n + BN - 1) / BN);
     const unsigned grid = static_cast<unsigned>(tiles < sms ? tiles : sms);
-    if (g.a) {
-        auto k = gemm_tc_kernel<true>;
-        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    auto run = [&](auto kern) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
         if (e != cudaSuccess) return e;
-        k<<<grid, THREADS, SMEM_BYTES, stream>>>(ta, tb, ty, p);
-    } else {
-        auto k = gemm_tc_kernel<false>;
-        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        k<<<grid, THREADS, SMEM_BYTES, stream>>>(ta, tb, ty, p);
-    }
-    return cudaGetLastError();
+        kern<<<grid, THREADS, SMEM_BYTES, stream>>>(ta, tb, ty, p);
+        return cudaGetLastError();
+    };
+    if (g.a) return run(gemm_tc_kernel<true, 0>);
+    if (p.act == 1) return run(gemm_tc_kernel<false, 1>);
+    if (p.act == 2) return run(gemm_tc_kernel<false, 2>);
+    return run(gemm_tc_kernel<false, 0>);
 }
 
 }  // namespace convrot

@@ -38,7 +38,22 @@ struct GemmArgs {
     int32_t *a;        // [m, ldy] (raw int32 output) or null
     int64_t ldy;
     int32_t *dev_status;
+    int32_t act;       // convrot_activation applied to Y (not to raw int32 output)
 };
+
+// GELU, erf or tanh form (convrot_activation), on the epilogue's fp32 value.
+__device__ __forceinline__ float apply_act(float v, int act)
+{
+    if (act == 1) return 0.5f * v * (1.0f + erff(v * 0.70710678118654752f));
+    if (act == 2) return 0.5f * v * (1.0f + tanhf(0.79788456080286536f * fmaf(0.044715f * v, v * v, v)));
+    return v;
+}
+
+template <int kAct>
+__device__ __forceinline__ float apply_act_t(float v)
+{
+    return kAct == 0 ? v : apply_act(v, kAct);
+}
 
 cudaError_t launch_gemm_imma(const GemmArgs &a, cudaStream_t stream);
 cudaError_t launch_gemm_tc(const GemmArgs &a, cudaStream_t stream);

@@ -38,12 +38,19 @@ class Workload:
     outlier_cols: tuple | None = None  # fixed columns; overrides outlier_frac
     gelu_input: bool = False  # X = GELU(N(0,1)) before the outlier scaling
     linears: int = 1  # linears sharing one packed X (q, k, v -> 3)
+    act: int = 0      # activation after the (first) linear: 0 none, 1 GELU erf form, 2 GELU tanh form
+    down_n: int = 0   # > 0: a DiT MLP pair; the activated output feeds a down projection to down_n features
     notes: str = field(default="", compare=False)
 
     @property
     def int_ops(self) -> int:
         """2*M*N*K integer operations of one GEMM."""
         return 2 * self.m * self.n * self.k
+
+    @property
+    def step_ops(self) -> int:
+        """2*M*N*K summed over every GEMM of one step (all linears, both MLP projections)."""
+        return sum(2 * self.m * st.n * st.k for st in stage_shapes(self))
 
     @property
     def pack_bytes(self) -> int:
@@ -92,6 +99,36 @@ def bias(wl: Workload, index: int = 0) -> np.ndarray:
     return rng.standard_normal((wl.n,), dtype=np.float32) * np.float32(0.01)
 
 
+@dataclass(frozen=True)
+class StageShape:
+    k: int   # input features
+    n: int   # output features (all linears of the stage)
+    act: int
+
+
+def stage_shapes(wl: Workload):
+    """The pack + linear stages of one step: one for a single (or grouped) linear,
+    two for an MLP pair (the second packs the first's activated output)."""
+    if wl.down_n:
+        return [StageShape(wl.k, wl.n, wl.act), StageShape(wl.n, wl.down_n, 0)]
+    return [StageShape(wl.k, wl.n * wl.linears, wl.act)]
+
+
+_DOWN = 10  # substream index of the down projection's weights and bias
+
+
+def stage_weights(wl: Workload, s: int):
+    """(list of W_i fp32 [n_i, k], concatenated bias fp32 [n]) of stage s."""
+    if s == 1:
+        W = np.random.default_rng(list(wl.seed) + [_TAG_W, _DOWN]).standard_normal(
+            (wl.down_n, wl.n), dtype=np.float32) * np.float32(0.02)
+        b = np.random.default_rng(list(wl.seed) + [_TAG_B, _DOWN]).standard_normal(
+            (wl.down_n,), dtype=np.float32) * np.float32(0.01)
+        return [W], b
+    count = 1 if wl.down_n else wl.linears
+    return [weights(wl, i) for i in range(count)], np.concatenate([bias(wl, i) for i in range(count)])
+
+
 def _sweep(G: int) -> Workload:
     return Workload(f"sweep_G{G}", 4096, 3072, 3072, G, (3, G))
 
@@ -103,6 +140,8 @@ WORKLOADS = {
         Workload("attn_qkv", 4096, 3072, 3072, 256, (1,), linears=3),
         Workload("mlp_up", 4096, 3072, 12288, 256, (2, 0)),
         Workload("mlp_down", 4096, 12288, 3072, 256, (2, 1), gelu_input=True),
+        Workload("mlp_pair", 4096, 3072, 12288, 256, (2, 2), act=1, down_n=3072,
+                 notes="up projection with GELU fused in its epilogue, then pack + down projection"),
         *[_sweep(G) for G in (4, 16, 64, 256, 1024)],
         Workload("video_n5120", 32760, 5120, 5120, 256, (4,), outlier_frac=0.0005,
                  outlier_scale=100.0),

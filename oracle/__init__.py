@@ -70,6 +70,8 @@ def _load():
         lib.oracle_reconstruct.restype = None
         lib.oracle_pack_rows.argtypes = [vp, i64, i64, i64, i64, vp, vp, i64, vp]
         lib.oracle_pack_rows.restype = ctypes.c_int
+        lib.oracle_activation.argtypes = [vp, i64, ctypes.c_int]
+        lib.oracle_activation.restype = None
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = ctypes.c_int
         _lib = lib
@@ -186,8 +188,15 @@ def gemm_i32(Qx: np.ndarray, Qw: np.ndarray, k: int) -> np.ndarray:
     return A
 
 
-def reconstruct(A: np.ndarray, sx: np.ndarray, sw: np.ndarray, bias: np.ndarray | None):
-    """Y = A * s_x[r] * s_w[o] + b[o] in fp64; returns (Y fp32, Y fp64)."""
+def activation(v: np.ndarray, act: int) -> np.ndarray:
+    """GELU (act 1: erf form, 2: tanh form) or identity (0) in fp64, elementwise."""
+    out = np.ascontiguousarray(v, dtype=np.float64).copy()
+    _load().oracle_activation(_ptr(out), out.size, int(act))
+    return out
+
+
+def reconstruct(A: np.ndarray, sx: np.ndarray, sw: np.ndarray, bias: np.ndarray | None, act: int = 0):
+    """Y = act(A * s_x[r] * s_w[o] + b[o]) in fp64; returns (Y fp32, Y fp64)."""
     A = np.ascontiguousarray(A, dtype=np.int32)
     sx = np.ascontiguousarray(sx, dtype=np.float32)
     sw = np.ascontiguousarray(sw, dtype=np.float32)
@@ -197,11 +206,14 @@ def reconstruct(A: np.ndarray, sx: np.ndarray, sw: np.ndarray, bias: np.ndarray 
     Y64 = np.empty((m, n), np.float64)
     _load().oracle_reconstruct(_ptr(A), n, m, n, _ptr(sx), _ptr(sw), _ptr(b), _ptr(Y), n,
                                _ptr(Y64))
+    if act:
+        Y64 = activation(Y64, act)
+        Y = Y64.astype(np.float32)
     return Y, Y64
 
 
-def linear(X: np.ndarray, W: np.ndarray, bias: np.ndarray | None, G: int):
-    """End to end: pack X, quantize W, integer GEMM, reconstruct.
+def linear(X: np.ndarray, W: np.ndarray, bias: np.ndarray | None, G: int, act: int = 0):
+    """End to end: pack X, quantize W, integer GEMM, reconstruct (then the activation).
 
     Returns a dict with Qx, sx, vx (pre-round), Qw, sw, A, Y (fp32), Y64.
     """
@@ -211,5 +223,5 @@ def linear(X: np.ndarray, W: np.ndarray, bias: np.ndarray | None, G: int):
     Qx, sx, vx = pack_rows(X, G)
     Qw, sw, _ = pack_rows(W, G, want_pre_round=False)
     A = gemm_i32(Qx, Qw, k)
-    Y, Y64 = reconstruct(A, sx, sw, bias)
+    Y, Y64 = reconstruct(A, sx, sw, bias, act)
     return {"Qx": Qx, "sx": sx, "vx": vx, "Qw": Qw, "sw": sw, "A": A, "Y": Y, "Y64": Y64}

@@ -37,6 +37,7 @@
  * Rows are independent; when compiled with -fopenmp the row loops run in
  * parallel. Results do not depend on the thread count.
  */
+#define _GNU_SOURCE
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
@@ -246,6 +247,27 @@ void oracle_reconstruct(const int32_t *A, int64_t lda, int64_t m, int64_t n, con
             if (Y_f64) Y_f64[r * n + o] = y;
             Y[r * ldy + o] = (float)y;
         }
+    }
+}
+
+/*
+ * Activation after the linear, for the up projection of a DiT MLP (the page's
+ * layer is a plain linear; the MLP applies GELU to its output before the down
+ * projection packs it). GELU(v) = v * Phi(v), Phi the standard normal CDF
+ * (Hendrycks and Gimpel, "Gaussian Error Linear Units"):
+ *   act 1: 0.5 v (1 + erf(v / sqrt 2))                       (exact form)
+ *   act 2: 0.5 v (1 + tanh(sqrt(2 / pi) (v + 0.044715 v^3)))  (their tanh approximation)
+ *   act 0: v
+ * Applied in place to count fp64 values.
+ */
+void oracle_activation(double *v, int64_t count, int act)
+{
+    for (int64_t i = 0; i < count; i++) {
+        const double x = v[i];
+        if (act == 1)
+            v[i] = 0.5 * x * (1.0 + erf(x / sqrt(2.0)));
+        else if (act == 2)
+            v[i] = 0.5 * x * (1.0 + tanh(sqrt(2.0 / M_PI) * (x + 0.044715 * x * x * x)));
     }
 }
 

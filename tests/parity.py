@@ -64,6 +64,20 @@ def check_y_same_codes(y_gpu: np.ndarray, y64_ref: np.ndarray, A: np.ndarray, sx
     assert not bad.any(), f"{bad.sum()} outputs off; worst {np.max(err / np.maximum(base, 1e-300)):.3e}"
 
 
+def check_y_act_same_codes(y_gpu: np.ndarray, y64_ref: np.ndarray, A: np.ndarray, sx, sw, bias):
+    """Y = act(A s_x s_w + b), given identical codes: the pre-activation rule
+    (1e-6 of |A s_x s_w| + |b|) times GELU's largest slope (1.13), rounded up
+    to 1.5e-6, plus 3e-7 |Y| for erff/tanhf and the fp32 products after them."""
+    base = np.abs(A.astype(np.float64) * np.asarray(sx, np.float64)[:, None]
+                  * np.asarray(sw, np.float64)[None, :])
+    if bias is not None:
+        base = base + np.abs(np.asarray(bias, np.float64))[None, :]
+    err = np.abs(np.asarray(y_gpu, np.float64) - y64_ref)
+    tol = 1.5e-6 * base + 3e-7 * np.abs(y64_ref) + 1e-30
+    bad = err > tol
+    assert not bad.any(), f"{bad.sum()} outputs off; worst {np.max(err / tol):.3e} of the tolerance"
+
+
 def check_y_end_to_end(y_gpu: np.ndarray, y_ref: np.ndarray, qx=None, qw=None, sx=None, sw=None):
     """qx = (gpu codes, oracle codes) of the rows of X behind y, qw likewise for W,
     sx, sw the GPU's scales; without them no code may have flipped."""

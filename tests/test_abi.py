@@ -148,3 +148,12 @@ def test_gemm_i32_validation(lib):
     assert lib.convrot_gemm_i32(ctypes.byref(x), ctypes.byref(w), FAKE, 3, None, None) == cr.ERR_INVALID_ARG
     x, w = pair(mx=0)
     assert lib.convrot_gemm_i32(ctypes.byref(x), ctypes.byref(w), None, 4, None, None) == cr.OK
+
+
+def test_linear_act_rejects_unknown_activation(lib):
+    x, w = pair()
+    for act in (-1, 3, 99):
+        assert lib.convrot_linear_act(ctypes.byref(x), ctypes.byref(w), None, act, FAKE, 64, None, None) == \
+            cr.ERR_INVALID_ARG
+    x, w = pair(mx=0)
+    assert lib.convrot_linear_act(ctypes.byref(x), ctypes.byref(w), None, cr.ACT_GELU_ERF, None, 64, None, None) == cr.OK

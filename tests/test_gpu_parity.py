@@ -156,6 +156,66 @@ def test_empty_pack_and_linear():
     assert Y.shape == (0, 8)
 
 
+@pytest.mark.parametrize("act", [cr.ACT_GELU_ERF, cr.ACT_GELU_TANH], ids=["gelu_erf", "gelu_tanh"])
+@pytest.mark.parametrize("codes", GEMM_CODES, ids=GEMM_IDS)
+@pytest.mark.parametrize("m,n,k", [(200, 300, 640), (64, 1000, 256), (300, 512, 1024)])
+def test_linear_act_identical_codes(m, n, k, codes, act):
+    """GELU fused into the epilogue, on both GEMM kernels; N = 300 and 1000 end
+    in a ragged 32-column box."""
+    rng = np.random.default_rng(m + n + k + act)
+    Qx, Qw = random_codes(rng, m, k), random_codes(rng, n, k)
+    sx = rng.uniform(0.0001, 0.002, m).astype(np.float32)
+    sw = rng.uniform(0.0001, 0.002, n).astype(np.float32)
+    b = rng.standard_normal(n).astype(np.float32)
+    px = cr.packed_from_codes(to_dev(Qx), to_dev(sx), 64, codes)
+    pw = cr.packed_from_codes(to_dev(Qw), to_dev(sw), 64, codes)
+    Ybig = torch.full((m + 1, (n + 7) // 4 * 4), -3.0, dtype=torch.float32, device="cuda")
+    Y = cr.convrot_linear_act(px, pw, to_dev(b), act, out=Ybig[:m, :n])
+    torch.cuda.synchronize()
+    A_ref = oracle.gemm_i32(Qx, Qw, k)
+    _, Y64 = oracle.reconstruct(A_ref, sx, sw, b, act)
+    parity.check_y_act_same_codes(Y.cpu().numpy(), Y64, A_ref, sx, sw, b)
+    assert torch.all(Ybig[m:] == -3.0) and torch.all(Ybig[:, n:] == -3.0)
+    # the values span GELU's curved part, not only its linear tails
+    pre = oracle.reconstruct(A_ref, sx, sw, b)[1]
+    assert (np.abs(pre) < 2).mean() > 0.2
+
+
+def test_mlp_pair_stage_by_stage():
+    """A DiT MLP: pack X, up projection with GELU in the epilogue, pack its
+    output, down projection. Each stage is checked against the oracle given the
+    GPU's own input to that stage."""
+    rng = np.random.default_rng(77)
+    m, d, h, G = 300, 512, 2048, 256
+    X = special_rows(rng, m, d)
+    Wu = (0.05 * rng.standard_normal((h, d))).astype(np.float32)
+    bu = (0.1 * rng.standard_normal(h)).astype(np.float32)
+    Wd = (0.02 * rng.standard_normal((d, h))).astype(np.float32)
+    bd = (0.1 * rng.standard_normal(d)).astype(np.float32)
+    px = cr.convrot_pack_activations(to_dev(X), G, cr.CODES_BF16)
+    pu = cr.convrot_quantize_weights(to_dev(Wu), G, cr.CODES_BF16)
+    pdn = cr.convrot_quantize_weights(to_dev(Wd), G, cr.CODES_BF16)
+    H = cr.convrot_linear_act(px, pu, to_dev(bu), cr.ACT_GELU_ERF)
+    ph = cr.convrot_pack_activations(H, G, cr.CODES_BF16)
+    Y = cr.convrot_linear(ph, pdn, to_dev(bd))
+    torch.cuda.synchronize()
+    H_np = H.cpu().numpy()
+    # stage 1: up projection + GELU against the oracle end to end
+    ref1 = oracle.linear(X, Wu, bu, G, act=1)
+    Qu_ref, _, _ = oracle.pack_rows(Wu, G, want_pre_round=False)
+    parity.check_y_end_to_end(H_np, ref1["Y64"], (codes_np(px), ref1["Qx"]), (codes_np(pu), Qu_ref),
+                              px.scale.cpu().numpy(), pu.scale.cpu().numpy())
+    # stage 2: the pack of the GPU's hidden activations
+    Qh_ref, sh_ref, vh = oracle.pack_rows(H_np, G)
+    parity.check_scales(ph.scale.cpu().numpy(), sh_ref)
+    parity.check_codes(codes_np(ph), Qh_ref, vh)
+    # stage 3: down projection against the oracle from the same hidden activations
+    ref3 = oracle.linear(H_np, Wd, bd, G)
+    Qd_ref, _, _ = oracle.pack_rows(Wd, G, want_pre_round=False)
+    parity.check_y_end_to_end(Y.cpu().numpy(), ref3["Y64"], (codes_np(ph), ref3["Qx"]), (codes_np(pdn), Qd_ref),
+                              ph.scale.cpu().numpy(), pdn.scale.cpu().numpy())
+
+
 def random_codes(rng, rows, k, sat=False):
     if sat:
         return np.where(rng.random((rows, k)) < 0.5, -127, 127).astype(np.int8)

@@ -269,3 +269,47 @@ def test_strided_input_rows():
     X = big[:, :64]  # leading dimension 100
     np.testing.assert_array_equal(oracle.rotate_fast(X, 16),
                                   oracle.rotate_fast(np.ascontiguousarray(X), 16))
+
+
+# ---- GELU after the up projection (the DiT MLP; not part of the page's linear)
+
+def test_gelu_odd_part_is_identity():
+    """GELU(x) - GELU(-x) = x for both forms: x Phi(x) + x Phi(-x) = x, and the
+    tanh form keeps the same symmetry (tanh is odd)."""
+    x = np.linspace(-8, 8, 1601)
+    for act in (1, 2):
+        d = oracle.activation(x, act) - oracle.activation(-x, act)
+        np.testing.assert_allclose(d, x, rtol=0, atol=1e-14)
+
+
+def test_gelu_erf_matches_normal_table():
+    """GELU(x) = x Phi(x): Phi(1) = 0.84134, Phi(2) = 0.97725, Phi(0.5) = 0.69146
+    (standard normal table, five places)."""
+    x = np.array([1.0, 2.0, 0.5, -1.0])
+    phi = np.array([0.84134, 0.97725, 0.69146, 1 - 0.84134])
+    np.testing.assert_allclose(oracle.activation(x, 1), x * phi, rtol=0, atol=1e-5 * 2)
+
+
+def test_gelu_limits_and_slope_at_zero():
+    for act in (1, 2):
+        g = oracle.activation(np.array([0.0, 30.0, -30.0, 1e-6]), act)
+        assert g[0] == 0.0 and abs(g[1] - 30.0) < 1e-12 and abs(g[2]) < 1e-12
+        assert abs(g[3] / 1e-6 - 0.5) < 1e-6  # GELU'(0) = Phi(0) = 1/2
+
+
+def test_gelu_tanh_form_approximates_erf_form():
+    x = np.linspace(-6, 6, 2401)
+    err = np.abs(oracle.activation(x, 2) - oracle.activation(x, 1))
+    assert err.max() < 1e-3 and err.max() > 1e-6  # close, and not the same function
+
+
+def test_linear_with_activation_is_activation_of_linear():
+    rng = np.random.default_rng(41)
+    X = rng.standard_normal((5, 64)).astype(np.float32)
+    W = (0.1 * rng.standard_normal((7, 64))).astype(np.float32)
+    b = rng.standard_normal(7).astype(np.float32)
+    base = oracle.linear(X, W, b, 16)
+    for act in (1, 2):
+        got = oracle.linear(X, W, b, 16, act=act)
+        np.testing.assert_array_equal(got["A"], base["A"])
+        np.testing.assert_allclose(got["Y64"], oracle.activation(base["Y64"], act), rtol=0, atol=0)
