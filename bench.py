@@ -196,6 +196,8 @@ def cpu_baseline(wl, budget_s: float, steps: int = 1, warmup: int = 0):
 
 
 def workload_name(wl) -> str:
+    if wl.lora_r:
+        return f"{wl.name} M{wl.m} K{wl.k} N{wl.n} G{wl.G} + LoRA r{wl.lora_r} scale {wl.lora_scale:g}"
     if wl.down_n:
         return f"{wl.name} M{wl.m} K{wl.k} N{wl.n} (GELU in the epilogue) -> K{wl.n} N{wl.down_n} G{wl.G}"
     grouped = f"x{wl.linears} (one grouped GEMM)" if wl.linears > 1 else ""
@@ -267,23 +269,48 @@ def run_ours(args):
         del Ws
     n_out = stages[-1].n
     stream = torch.cuda.current_stream(dev)
+    if wl.lora_r:  # runtime LoRA on the first linear: T from the unrotated X, one extra GEMM chunk
+        A_l, B_l = inputs.lora_weights(wl)
+        A_l = cr.convrot_lora_prepare_down(torch.from_numpy(A_l).to(dev))
+        B_ext = cr.convrot_lora_prepare(torch.from_numpy(B_l).to(dev), wl.lora_scale)
+        T_ext = [torch.empty((wl.m, cr.lora_cols(wl.lora_r)), dtype=torch.bfloat16, device=dev) for _ in range(R)]
 
-    def run_stages(x_in, j, ev=None):
+    def run_stages(x_in, j, marks=None):
+        """One step; with marks (a list of (tag, event) slots) it records an event before
+        each kernel, tagged with the kernel, and one at the end."""
+        used = 0
+
+        def mark(tag):
+            nonlocal used
+            if marks is not None:
+                marks[used][1].record(stream)
+                marks[used][0] = tag
+                used += 1
+
         h = x_in
         for s_i, st in enumerate(stages):
-            if ev is not None:
-                ev[2 * s_i].record(stream)
+            if wl.lora_r and s_i == 0:
+                mark("lora_down")
+                cr.convrot_lora_down(h, A_l, out=T_ext[j], stream=stream)
+            mark("pack")
             cr.convrot_pack_activations(h, wl.G, codes, out=pxs[s_i][j], stream=stream)
-            if ev is not None:
-                ev[2 * s_i + 1].record(stream)
-            cr.convrot_linear_act(pxs[s_i][j], pws[s_i][j], biases[s_i], st.act, out=Ys[s_i][j], stream=stream)
+            mark("gemm")
+            if wl.lora_r and s_i == 0:
+                cr.convrot_linear_lora(pxs[s_i][j], pws[s_i][j], biases[s_i], st.act, T_ext[j], B_ext, wl.lora_r,
+                                       out=Ys[s_i][j], stream=stream)
+            else:
+                cr.convrot_linear_act(pxs[s_i][j], pws[s_i][j], biases[s_i], st.act, out=Ys[s_i][j],
+                                      stream=stream)
             h = Ys[s_i][j]
-        if ev is not None:
-            ev[2 * len(stages)].record(stream)
+        mark("end")
         return h
 
-    def step(i, ev=None):
-        run_stages(Xs[i % R], i % R, ev)
+    def step(i, marks=None):
+        run_stages(Xs[i % R], i % R, marks)
+
+    def kernel_ms(marks, tag):
+        """Milliseconds between each event tagged `tag` and the next event, summed."""
+        return sum(marks[i][1].elapsed_time(marks[i + 1][1]) for i in range(len(marks) - 1) if marks[i][0] == tag)
 
     for i in range(args.warmup):
         step(i)
@@ -301,7 +328,8 @@ def run_ours(args):
     clocks = ClockSampler(uuid)
     clocks.start()
     time.sleep(0.3)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * len(stages) + 1)] for _ in range(args.steps)]
+    n_marks = 2 * len(stages) + (1 if wl.lora_r else 0) + 1
+    evs = [[[None, torch.cuda.Event(enable_timing=True)] for _ in range(n_marks)] for _ in range(args.steps)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     # the timed loop runs several times over so the clock sampler sees a loaded GPU
@@ -314,8 +342,9 @@ def run_ours(args):
         pg.barrier()
     torch.cuda.synchronize(dev)
     total_ms = t_start.elapsed_time(t_end)
-    pack_ms = [sum(e[2 * k].elapsed_time(e[2 * k + 1]) for k in range(len(stages))) for e in evs]
-    gemm_ms = [sum(e[2 * k + 1].elapsed_time(e[2 * k + 2]) for k in range(len(stages))) for e in evs]
+    pack_ms = [kernel_ms(e, "pack") for e in evs]
+    gemm_ms = [kernel_ms(e, "gemm") for e in evs]
+    lora_ms = [kernel_ms(e, "lora_down") for e in evs] if wl.lora_r else None
     # keep the GPU busy a little longer with the same steps for the clock record
     t_keep = time.time()
     i = 0
@@ -371,6 +400,10 @@ def run_ours(args):
                    "codes": "i8" if codes == cr.CODES_I8 else "bf16",
                    "l2": f"{R} rotating input/output sets, {touched / 1e6:.0f} MB touched per step (> L2)"},
         "pack_gbs": pack_gbs, "pack_ms": pack_avg, "gemm_ms": gemm_avg, "gemm_tops": gemm_tops,
+        **({"lora_down_ms": sum(lora_ms) / len(lora_ms),
+            "lora": f"rank {wl.lora_r}, scale {wl.lora_scale:g}: T = X A^T in its own kernel (lora_down_ms), "
+                    "the correction as an extra fp32 chunk of the GEMM (in gemm_ms); its own "
+                    "multiply-adds are not counted in value"} if wl.lora_r else {}),
         "roofline": {"bound": "tensor", "achieved": gemm_tops, "peak": pk["bf16_tflops"],
                      "unit": "TFLOP/s", "frac": gemm_tops / pk["bf16_tflops"], "traffic": traffic,
                      "kernel": "gemm", "peak_source": f"{pk['source']} dense bf16 burst"},
@@ -380,7 +413,7 @@ def run_ours(args):
         "e2e": {"value": job_tops(world, ops, e2e_ms), "unit": "TOPS",
                 "h2d_bytes_per_step": wl.m * wl.k * 4, "d2h_bytes_per_step": wl.m * n_out * 4,
                 "ms_per_step": e2e_ms},
-        "gpu_launches": 2 * len(stages) * args.steps,
+        "gpu_launches": (2 * len(stages) + (1 if wl.lora_r else 0)) * args.steps,
         "clocks": clk,
     }
     if not args.no_cpu_baseline and world == 1:

@@ -171,6 +171,68 @@ convrot_status convrot_linear_act(const convrot_packed *x, const convrot_packed 
                                   cudaStream_t stream);
 
 /*
+ * Runtime LoRA side branch (page "INT8 Convrot Safetensors", "Backend
+ * support", paragraph on adapters): the INT8 weights stay as they are, and
+ * the adapter's correction is computed from the original, unrotated
+ * activation and added to the linear's output:
+ *   Y = act(A s_x s_w + b + scale * (X A_lora^T) B_lora^T)
+ * with A_lora [r, k] (down) and B_lora [n, r] (up). The correction runs on the
+ * tensor cores in split precision (T = X A_lora^T with three-term TF32, then
+ * T B^T with two-term bf16 on both sides), close to an fp32 computation.
+ *
+ * convrot_lora_cols(r): the K extent of the extended operands, 3 r rounded up
+ * to 64 (0 for an r that is not accepted). r must be a multiple of 16 in
+ * [16, 256].
+ */
+int64_t convrot_lora_cols(int32_t r);
+
+/*
+ * Offline, once per adapter: B_ext [n, lde] bf16 =
+ * [hi(scale B) | lo(scale B) | hi(scale B) | 0 ...], hi = bf16(v),
+ * lo = bf16(v - hi).
+ *   B       device fp32 [n, ldb], 4-byte aligned, ldb >= r.
+ *   scale   the adapter's scale (alpha / r in the usual files).
+ *   B_ext   device, 16-byte aligned, lde >= convrot_lora_cols(r), lde % 8 == 0.
+ */
+convrot_status convrot_lora_prepare(const float *B, int64_t n, int32_t r, int64_t ldb, float scale,
+                                    void *B_ext, int64_t lde, cudaStream_t stream);
+
+/*
+ * Offline, once per adapter: A_ext [2r, lde] fp32 = [hi(A); lo(A)], hi = A with
+ * its low 13 mantissa bits cleared (exact in TF32), lo = A - hi.
+ *   A       device fp32 [r, lda], 4-byte aligned, lda >= k, 1 <= k <= CONVROT_MAX_K.
+ *   A_ext   device, 16-byte aligned, lde >= k, lde % 4 == 0.
+ */
+convrot_status convrot_lora_prepare_down(const float *A, int32_t r, int64_t k, int64_t lda, float *A_ext,
+                                         int64_t lde, cudaStream_t stream);
+
+/*
+ * Per call: T = X A_lora^T from the unrotated X, written as
+ * T_ext [m, ldt] bf16 = [hi(T) | hi(T) | lo(T) | 0 ...].
+ *   X       device fp32 [m, ldx] (the same X the pack reads), 16-byte aligned,
+ *           ldx >= k, ldx % 4 == 0; 1 <= k <= CONVROT_MAX_K.
+ *   A_ext   from convrot_lora_prepare_down: device fp32 [2r, lda], 16-byte
+ *           aligned, lda >= k, lda % 4 == 0.
+ *   T_ext   device, 16-byte aligned, ldt >= convrot_lora_cols(r), ldt % 8 == 0.
+ *   dev_status  as for convrot_linear (the kernel waits on its copies with a
+ *               4 s bound).
+ */
+convrot_status convrot_lora_down(const float *X, int64_t m, int64_t k, int64_t ldx, const float *A_ext, int32_t r,
+                                 int64_t lda, void *T_ext, int64_t ldt, int32_t *dev_status, cudaStream_t stream);
+
+/*
+ * The linear with the LoRA correction added in its epilogue (bf16 codes only;
+ * I8 codes give CONVROT_ERR_UNSUPPORTED): Y = act(base + T_ext B_ext^T).
+ *   T_ext, ldt  from convrot_lora_down on this x's activations (x->rows rows).
+ *   B_ext, lde  from convrot_lora_prepare (w->rows rows).
+ *   r           the adapter's rank, as given to both.
+ * Everything else as for convrot_linear_act.
+ */
+convrot_status convrot_linear_lora(const convrot_packed *x, const convrot_packed *w, const float *bias, int32_t act,
+                                   const void *T_ext, int64_t ldt, const void *B_ext, int64_t lde, int32_t r,
+                                   float *Y, int64_t ldy, int32_t *dev_status, cudaStream_t stream);
+
+/*
  * The integer GEMM alone: A[r, o] = sum_i Q_x[r, i] * Q_w[o, i] as int32, for
  * checking the accumulation bit for bit. Same operand rules as
  * convrot_linear.

@@ -28,6 +28,11 @@ EXPORTED = [
     "convrot_pack_activations",
     "convrot_linear",
     "convrot_linear_act",
+    "convrot_lora_cols",
+    "convrot_lora_prepare",
+    "convrot_lora_prepare_down",
+    "convrot_lora_down",
+    "convrot_linear_lora",
     "convrot_gemm_i32",
     "convrot_status_string",
 ]
@@ -81,6 +86,16 @@ def load() -> ctypes.CDLL:
         lib.convrot_linear.restype = ctypes.c_int
         lib.convrot_linear_act.argtypes = [P, P, vp, i32, vp, i64, vp, vp]
         lib.convrot_linear_act.restype = ctypes.c_int
+        lib.convrot_lora_cols.argtypes = [i32]
+        lib.convrot_lora_cols.restype = i64
+        lib.convrot_lora_prepare.argtypes = [vp, i64, i32, i64, ctypes.c_float, vp, i64, vp]
+        lib.convrot_lora_prepare.restype = ctypes.c_int
+        lib.convrot_lora_prepare_down.argtypes = [vp, i32, i64, i64, vp, i64, vp]
+        lib.convrot_lora_prepare_down.restype = ctypes.c_int
+        lib.convrot_lora_down.argtypes = [vp, i64, i64, i64, vp, i32, i64, vp, i64, vp, vp]
+        lib.convrot_lora_down.restype = ctypes.c_int
+        lib.convrot_linear_lora.argtypes = [P, P, vp, i32, vp, i64, vp, i64, i32, vp, i64, vp, vp]
+        lib.convrot_linear_lora.restype = ctypes.c_int
         lib.convrot_gemm_i32.argtypes = [P, P, vp, i64, vp, vp]
         lib.convrot_gemm_i32.restype = ctypes.c_int
         lib.convrot_status_string.argtypes = [ctypes.c_int]
@@ -212,6 +227,76 @@ def convrot_linear_act(x: Packed, w: Packed, bias: torch.Tensor | None, act: int
     _check(load().convrot_linear_act(ctypes.byref(xs), ctypes.byref(ws), _ptr(bias), int(act), _ptr(out),
                                      out.stride(0) if out.dim() == 2 else 0, _ptr(dev_status),
                                      _stream(stream)), "convrot_linear_act")
+    return out
+
+
+def lora_cols(r: int) -> int:
+    """K extent of the LoRA operands: 3 r rounded up to 64 (0 if r is not accepted)."""
+    return int(load().convrot_lora_cols(int(r)))
+
+
+def _lora_out(rows: int, r: int, device) -> torch.Tensor:
+    cols = lora_cols(r)
+    if cols == 0:
+        raise ConvrotError(ERR_INVALID_ARG, "lora rank")
+    return torch.empty((rows, cols), dtype=torch.bfloat16, device=device)
+
+
+def convrot_lora_prepare(B: torch.Tensor, scale: float, out: torch.Tensor | None = None,
+                         stream=None) -> torch.Tensor:
+    """Offline: B [n, r] fp32 (the adapter's up matrix) -> B_ext [n, lora_cols(r)] bf16 with
+    the scale folded in."""
+    if B.dtype != torch.float32 or not B.is_cuda or B.dim() != 2 or B.stride(1) != 1:
+        raise TypeError("B must be a 2-D row-major float32 CUDA tensor")
+    n, r = B.shape
+    if out is None:
+        out = _lora_out(n, r, B.device)
+    _check(load().convrot_lora_prepare(_ptr(B), n, r, B.stride(0), float(scale), _ptr(out), out.stride(0),
+                                       _stream(stream)), "convrot_lora_prepare")
+    return out
+
+
+def convrot_lora_prepare_down(A: torch.Tensor, stream=None) -> torch.Tensor:
+    """Offline: the adapter's down matrix A [r, k] fp32 -> A_ext [2r, k rounded up to 4] fp32
+    = [hi(A); lo(A)] (hi exact in TF32)."""
+    if A.dtype != torch.float32 or not A.is_cuda or A.dim() != 2 or A.stride(1) != 1:
+        raise TypeError("A must be a 2-D row-major float32 CUDA tensor")
+    r, k = A.shape
+    out = torch.zeros((2 * r, (k + 3) // 4 * 4), dtype=torch.float32, device=A.device)
+    _check(load().convrot_lora_prepare_down(_ptr(A), r, k, A.stride(0), _ptr(out), out.stride(0), _stream(stream)),
+           "convrot_lora_prepare_down")
+    return out
+
+
+def convrot_lora_down(X: torch.Tensor, A_ext: torch.Tensor, out: torch.Tensor | None = None,
+                      dev_status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Per call: T = X A^T from the unrotated X [m, k] and A_ext (convrot_lora_prepare_down),
+    as T_ext [m, lora_cols(r)] bf16."""
+    for t, name in ((X, "X"), (A_ext, "A_ext")):
+        if t.dtype != torch.float32 or not t.is_cuda or t.dim() != 2 or t.stride(1) != 1:
+            raise TypeError(f"{name} must be a 2-D row-major float32 CUDA tensor")
+    m, k = X.shape
+    r = A_ext.shape[0] // 2
+    if out is None:
+        out = _lora_out(m, r, X.device)
+    _check(load().convrot_lora_down(_ptr(X), m, k, X.stride(0), _ptr(A_ext), r, A_ext.stride(0), _ptr(out),
+                                    out.stride(0), _ptr(dev_status), _stream(stream)), "convrot_lora_down")
+    return out
+
+
+def convrot_linear_lora(x: Packed, w: Packed, bias: torch.Tensor | None, act: int, t_ext: torch.Tensor,
+                        b_ext: torch.Tensor, r: int, out: torch.Tensor | None = None,
+                        dev_status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Y = act((Q_x Q_w^T) s_x s_w + b + T_ext B_ext^T): the linear with the LoRA correction."""
+    if out is None:
+        out = _padded_out(x.rows, w.rows, torch.float32, x.q.device)
+    if bias is not None and (bias.dtype != torch.float32 or not bias.is_cuda):
+        raise TypeError("bias must be a float32 CUDA tensor")
+    xs, ws = x.struct(), w.struct()
+    _check(load().convrot_linear_lora(ctypes.byref(xs), ctypes.byref(ws), _ptr(bias), int(act), _ptr(t_ext),
+                                      t_ext.stride(0), _ptr(b_ext), b_ext.stride(0), int(r), _ptr(out),
+                                      out.stride(0) if out.dim() == 2 else 0, _ptr(dev_status), _stream(stream)),
+           "convrot_linear_lora")
     return out
 
 

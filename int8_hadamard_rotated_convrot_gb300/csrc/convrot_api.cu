@@ -96,14 +96,36 @@ convrot_status check_pair(const convrot_packed *x, const convrot_packed *w)
     return check_packed_buffers(w, w->rows, w->k);
 }
 
+struct LoraArgs {
+    int32_t r = 0;
+    const void *t = nullptr;
+    int64_t ldt = 0;
+    const void *b = nullptr;
+    int64_t ldb = 0;
+};
+
+bool lora_rank_ok(int32_t r) { return r >= 16 && r <= 256 && r % 16 == 0; }
+
 convrot_status run_gemm(const convrot_packed *x, const convrot_packed *w, const float *bias, float *Y,
-                        int32_t *A, int64_t ld, int32_t act, int32_t *dev_status, cudaStream_t stream)
+                        int32_t *A, int64_t ld, int32_t act, int32_t *dev_status, cudaStream_t stream,
+                        const LoraArgs &lora = LoraArgs{})
 {
     if (act < CONVROT_ACT_NONE || act > CONVROT_ACT_GELU_TANH) return CONVROT_ERR_INVALID_ARG;
     convrot_status st = check_pair(x, w);
     if (st != CONVROT_OK) return st;
     const int64_t m = x->rows, n = w->rows;
     if (ld < n) return CONVROT_ERR_INVALID_ARG;
+    if (lora.r != 0) {
+        if (!lora_rank_ok(lora.r)) return CONVROT_ERR_INVALID_ARG;
+        if (x->codes != CONVROT_CODES_BF16) return CONVROT_ERR_UNSUPPORTED;
+        const int64_t cols = (3 * int64_t{lora.r} + 63) / 64 * 64;
+        if (lora.ldt < cols || lora.ldb < cols) return CONVROT_ERR_INVALID_ARG;
+        if (m > 0 && n > 0) {
+            if (!lora.t || !lora.b) return CONVROT_ERR_INVALID_ARG;
+            if (!aligned(lora.t, 16) || !aligned(lora.b, 16) || lora.ldt % 8 || lora.ldb % 8)
+                return CONVROT_ERR_ALIGNMENT;
+        }
+    }
     if (m > 0 && n > 0) {
         void *out = Y ? static_cast<void *>(Y) : static_cast<void *>(A);
         if (!out) return CONVROT_ERR_INVALID_ARG;
@@ -129,6 +151,11 @@ convrot_status run_gemm(const convrot_packed *x, const convrot_packed *w, const 
     g.ldy = ld;
     g.dev_status = dev_status;
     g.act = act;
+    g.lora_r = lora.r;
+    g.lora_t = lora.t;
+    g.lora_ldt = lora.ldt;
+    g.lora_b = lora.b;
+    g.lora_ldb = lora.ldb;
     cudaError_t e = x->codes == CONVROT_CODES_I8 ? convrot::launch_gemm_imma(g, stream)
                                                  : convrot::launch_gemm_tc(g, stream);
     if (e == cudaErrorNotSupported) return CONVROT_ERR_UNSUPPORTED;
@@ -165,6 +192,63 @@ convrot_status convrot_linear_act(const convrot_packed *x, const convrot_packed 
 {
     if (!Y && x && w && x->rows > 0 && w->rows > 0) return CONVROT_ERR_INVALID_ARG;
     return run_gemm(x, w, bias, Y, nullptr, ldy, act, dev_status, stream);
+}
+
+int64_t convrot_lora_cols(int32_t r) { return lora_rank_ok(r) ? (3 * int64_t{r} + 63) / 64 * 64 : 0; }
+
+convrot_status convrot_lora_prepare(const float *B, int64_t n, int32_t r, int64_t ldb, float scale, void *B_ext,
+                                    int64_t lde, cudaStream_t stream)
+{
+    if (!lora_rank_ok(r) || n < 0 || ldb < r || lde < convrot_lora_cols(r)) return CONVROT_ERR_INVALID_ARG;
+    if (n == 0) return CONVROT_OK;
+    if (!B || !B_ext) return CONVROT_ERR_INVALID_ARG;
+    if (!aligned(B, 4) || !aligned(B_ext, 16) || lde % 8 != 0) return CONVROT_ERR_ALIGNMENT;
+    return convrot::launch_lora_prepare(B, n, r, ldb, scale, B_ext, lde, stream) == cudaSuccess ? CONVROT_OK
+                                                                                               : CONVROT_ERR_CUDA;
+}
+
+convrot_status convrot_lora_prepare_down(const float *A, int32_t r, int64_t k, int64_t lda, float *A_ext,
+                                         int64_t lde, cudaStream_t stream)
+{
+    if (!lora_rank_ok(r)) return CONVROT_ERR_INVALID_ARG;
+    if (k < 1 || k > CONVROT_MAX_K) return CONVROT_ERR_K_RANGE;
+    if (lda < k || lde < k) return CONVROT_ERR_INVALID_ARG;
+    if (!A || !A_ext) return CONVROT_ERR_INVALID_ARG;
+    if (!aligned(A, 4) || !aligned(A_ext, 16) || lde % 4 != 0) return CONVROT_ERR_ALIGNMENT;
+    return convrot::launch_lora_prepare_down(A, r, static_cast<int32_t>(k), lda, A_ext, lde, stream) == cudaSuccess
+               ? CONVROT_OK
+               : CONVROT_ERR_CUDA;
+}
+
+convrot_status convrot_lora_down(const float *X, int64_t m, int64_t k, int64_t ldx, const float *A, int32_t r,
+                                 int64_t lda, void *T_ext, int64_t ldt, int32_t *dev_status, cudaStream_t stream)
+{
+    if (!lora_rank_ok(r) || m < 0 || ldt < convrot_lora_cols(r)) return CONVROT_ERR_INVALID_ARG;
+    if (k < 1 || k > CONVROT_MAX_K) return CONVROT_ERR_K_RANGE;
+    if (ldx < k || lda < k || ldx % 4 != 0 || lda % 4 != 0) return CONVROT_ERR_INVALID_ARG;
+    if (m == 0) return CONVROT_OK;
+    if (!X || !A || !T_ext) return CONVROT_ERR_INVALID_ARG;
+    if (!aligned(X, 16) || !aligned(A, 16) || !aligned(T_ext, 16) || ldt % 8 != 0) return CONVROT_ERR_ALIGNMENT;
+    if (dev_status && !aligned(dev_status, 4)) return CONVROT_ERR_ALIGNMENT;
+    return convrot::launch_lora_down(X, m, static_cast<int32_t>(k), ldx, A, r, lda, T_ext, ldt, dev_status, stream) ==
+                   cudaSuccess
+               ? CONVROT_OK
+               : CONVROT_ERR_CUDA;
+}
+
+convrot_status convrot_linear_lora(const convrot_packed *x, const convrot_packed *w, const float *bias, int32_t act,
+                                   const void *T_ext, int64_t ldt, const void *B_ext, int64_t lde, int32_t r,
+                                   float *Y, int64_t ldy, int32_t *dev_status, cudaStream_t stream)
+{
+    if (!Y && x && w && x->rows > 0 && w->rows > 0) return CONVROT_ERR_INVALID_ARG;
+    if (r == 0) return CONVROT_ERR_INVALID_ARG;
+    LoraArgs lora;
+    lora.r = r;
+    lora.t = T_ext;
+    lora.ldt = ldt;
+    lora.b = B_ext;
+    lora.ldb = lde;
+    return run_gemm(x, w, bias, Y, nullptr, ldy, act, dev_status, stream, lora);
 }
 
 convrot_status convrot_gemm_i32(const convrot_packed *x, const convrot_packed *w, int32_t *A,

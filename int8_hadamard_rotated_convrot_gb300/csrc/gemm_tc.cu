@@ -36,9 +36,12 @@
 
 #include "../../include/convrot.h"
 #include "internal.h"
+#include "tc_common.cuh"
 
 namespace convrot {
 namespace {
+
+using namespace tc;
 
 constexpr int BM = 128, BN = 256, BK = 64;  // BK bf16 = 128 B = one swizzle span
 constexpr int STAGES = 3;
@@ -57,80 +60,10 @@ constexpr int OUT_BUF_BYTES = OUT_BOX * OUT_BOX * 4;
 constexpr int OUT_WARP_BYTES = 2 * OUT_BUF_BYTES;
 constexpr int OUT_BYTES = 8 * OUT_WARP_BYTES;
 constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + OUT_BYTES + BAR_BYTES;
-constexpr uint64_t kTimeoutNs = 4000000000ull;  // 4 s
 
 // instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major, M = 128, N = 256
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(BN >> 3) << 17) |
                             (uint32_t(BM >> 4) << 24);
-
-__device__ __forceinline__ uint64_t globaltimer()
-{
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
-{
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Waits for the phase with the given parity; false if it did not come within the limit.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
-{
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer();
-    for (;;) {
-#pragma unroll 1
-        for (int i = 0; i < 32; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
-        if (globaltimer() - t0 > kTimeoutNs) return false;
-    }
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar)
-{
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
-{
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
-                                            uint32_t bar)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, "
-        "{%2, %3}], [%4];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-        : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart.
-__device__ __forceinline__ uint64_t smem_desc(uint32_t addr)
-{
-    return (uint64_t((addr >> 4) & 0x3fff)) | (uint64_t(1) << 16) | (uint64_t(1024 >> 4) << 32) |
-           (uint64_t(1) << 46) | (uint64_t(2) << 61);
-}
 
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t accumulate)
 {
@@ -142,27 +75,6 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b
         : "memory");
 }
 
-__device__ __forceinline__ void mma_commit(uint32_t bar)
-{
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-                 : "memory");
-}
-
-// 32 lanes x 32 consecutive 32-bit columns; thread i of the warp gets lane (base + i).
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32])
-{
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
-          "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
-          "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
 struct TcParams {
     int64_t m, n;
     int32_t vec_cols;  // s_w and bias are 16-byte aligned
@@ -172,7 +84,8 @@ struct TcParams {
     int32_t *a;
     int64_t ldy;
     int32_t *dev_status;
-    int32_t act;  // convrot_activation on Y
+    int32_t act;       // convrot_activation on Y
+    int32_t lora_kst;  // 64-wide K slices of the LoRA operands (pair kernel, kLora)
 };
 
 
@@ -202,10 +115,13 @@ __device__ __forceinline__ void act_box(uint32_t buf, int lane)
     }
 }
 
-template <bool kRawInt32, int kAct>
+// With kLora, lora_taddr is the TMEM address of this warp's rows and columns
+// of the LoRA chunk (fp32), added to each output before the activation.
+template <bool kRawInt32, int kAct, bool kLora = false>
 __device__ __forceinline__ void store_tile_rows(const TcParams &p, const CUtensorMap *tmY, uint32_t out_smem,
                                                 uint32_t &store_iter, int64_t row0, int64_t col0,
-                                                const int32_t (&acc)[128], int lane, int ncols = 128)
+                                                const int32_t (&acc)[128], int lane, int ncols = 128,
+                                                uint32_t lora_taddr = 0)
 {
     const int64_t row = row0 + lane;
     float sxr = 0.0f;
@@ -215,8 +131,10 @@ __device__ __forceinline__ void store_tile_rows(const TcParams &p, const CUtenso
         if (cc * 32 >= ncols) break;
         const int64_t x = col0 + cc * 32;
         if (x >= p.n) break;
-        if (kAct != 0 && x + 32 > p.n) {
-            // ragged last box with an activation: stage, activate, then masked stores from shared memory
+        uint32_t lr[kLora ? 32 : 1];
+        if constexpr (kLora) tmem_ld32(lora_taddr + cc * 32, lr);
+        if ((kAct != 0 || kLora) && x + 32 > p.n) {
+            // ragged last box with an activation or a LoRA term: stage, activate, then masked stores
             const uint32_t buf = out_smem + (store_iter & 1u) * OUT_BUF_BYTES;
             if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
             __syncwarp();
@@ -228,14 +146,16 @@ __device__ __forceinline__ void store_tile_rows(const TcParams &p, const CUtenso
                     const int64_t col = x + c * 4 + e;
                     const float swv = col < p.n ? __ldg(p.sw + col) : 0.0f;
                     const float bv = (p.bias && col < p.n) ? __ldg(p.bias + col) : 0.0f;
-                    w[e] = __float_as_uint(fmaf(static_cast<float>(acc[cc * 32 + c * 4 + e]) * sxr, swv, bv));
+                    float y = fmaf(static_cast<float>(acc[cc * 32 + c * 4 + e]) * sxr, swv, bv);
+                    if constexpr (kLora) y += __uint_as_float(lr[c * 4 + e]);
+                    w[e] = __float_as_uint(y);
                 }
                 const uint32_t addr = buf + lane * (OUT_BOX * 4) + ((c ^ (lane & 7)) << 4);
                 asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[0]), "r"(w[1]), "r"(w[2]),
                              "r"(w[3])
                              : "memory");
             }
-            act_box<kAct>(buf, lane);
+            if constexpr (kAct != 0) act_box<kAct>(buf, lane);
             if (row < p.m) {
 #pragma unroll 1
                 for (int j = 0; j < 32 && x + j < p.n; ++j) {
@@ -286,10 +206,13 @@ __device__ __forceinline__ void store_tile_rows(const TcParams &p, const CUtenso
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int j = cc * 32 + c * 4 + e;
-                if constexpr (kRawInt32)
+                if constexpr (kRawInt32) {
                     w[e] = static_cast<uint32_t>(acc[j]);
-                else
-                    w[e] = __float_as_uint(fmaf(static_cast<float>(acc[j]) * sxr, swv[e], bv[e]));
+                } else {
+                    float y = fmaf(static_cast<float>(acc[j]) * sxr, swv[e], bv[e]);
+                    if constexpr (kLora) y += __uint_as_float(lr[c * 4 + e]);
+                    w[e] = __float_as_uint(y);
+                }
             }
             const uint32_t addr = buf + lane * (OUT_BOX * 4) + ((c ^ (lane & 7)) << 4);
             asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[0]), "r"(w[1]), "r"(w[2]),
@@ -603,10 +526,14 @@ __device__ __forceinline__ void arrive_remote(uint32_t cluster_bar)
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
 }
 
-template <int BN, bool kRawInt32, int kAct>
+// kLora: after each tile's K slices, the producer streams lora_kst more slices
+// from tmLa (T_ext rows) and tmLb (B_ext rows); the MMA runs them as one extra
+// chunk whose fp32 sums are not promoted to int32 but added to the output.
+template <int BN, bool kRawInt32, int kAct, bool kLora>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                        const __grid_constant__ CUtensorMap tmY, TcParams p)
+                        const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmLa,
+                        const __grid_constant__ CUtensorMap tmLb, TcParams p)
 {
     using C = Cfg<BN>;
     constexpr int STAGES = C::STAGES, STAGE_BYTES = C::STAGE_BYTES, A_BYTES = C::A_BYTES, BNP = C::BNP, BNC = C::BNC;
@@ -632,6 +559,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     const int64_t pair_id = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
     const int kst = p.kstages;
     const int n_chunks = (kst + CHUNK_KSTAGES - 1) / CHUNK_KSTAGES;
+    const int lkst = kLora ? p.lora_kst : 0;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -641,6 +569,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         for (int b = 0; b < 2; ++b) {
             mbar_init(accf_bar(b), 1);
             mbar_init(acce_bar(b), 2 * EPI_WARPS);
+        }
+        if constexpr (kLora) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmLa)) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmLb)) : "memory");
         }
         mbar_init(done_bar, 1);
         *abort_flag = 0;
@@ -676,7 +608,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                 const int mt = static_cast<int>(t % n_mt), nt = static_cast<int>(t / n_mt);
                 const int arow = mt * 2 * BMC + static_cast<int>(rank) * BMC;
                 const int brow = nt * BNP + static_cast<int>(rank) * BNC;
-                for (int ks = 0; ks < kst; ++ks) {
+                for (int ks = 0; ks < kst + lkst; ++ks) {
                     if (*abort_flag || !mbar_wait(empty_bar(stage), phase ^ 1u)) {
                         ok = false;
                         break;
@@ -684,8 +616,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                     const uint32_t sa = base + stage * STAGE_BYTES;
                     if (leader) mbar_arrive_expect_tx(full_bar(stage), 2 * STAGE_BYTES);
                     const uint32_t lbar = map_to_rank(full_bar(stage), 0);
-                    tma_load_2d_pair(sa, &tmA, ks * BK, arow, lbar);
-                    tma_load_2d_pair(sa + A_BYTES, &tmB, ks * BK, brow, lbar);
+                    const bool lo = kLora && ks >= kst;
+                    const int kx = (lo ? ks - kst : ks) * BK;
+                    tma_load_2d_pair(sa, lo ? &tmLa : &tmA, kx, arow, lbar);
+                    tma_load_2d_pair(sa + A_BYTES, lo ? &tmLb : &tmB, kx, brow, lbar);
                     ++issued;
                     if (++stage == STAGES) {
                         stage = 0;
@@ -715,7 +649,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             uint32_t chunk_iter = 0;
             bool ok = true;
             for (int64_t t = pair_id; t < n_tiles && ok; t += n_pairs) {
-                for (int c = 0; c < n_chunks && ok; ++c, ++chunk_iter) {
+                for (int c = 0; c < n_chunks + (kLora ? 1 : 0) && ok; ++c, ++chunk_iter) {
                     const uint32_t buf = chunk_iter & 1u;
                     if (*abort_flag || !mbar_wait(acce_bar(buf), ((chunk_iter >> 1) & 1u) ^ 1u)) {
                         ok = false;
@@ -723,8 +657,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                     }
                     tc_fence_after();
                     const uint32_t d_tmem = tmem_base + buf * BNP;
-                    const int ks0 = c * CHUNK_KSTAGES;
-                    const int ks1 = ks0 + CHUNK_KSTAGES < kst ? ks0 + CHUNK_KSTAGES : kst;
+                    // integer chunks of up to 1024 K, then (kLora) the LoRA slices as one chunk
+                    const int ks0 = c < n_chunks ? c * CHUNK_KSTAGES : kst;
+                    const int ks1 = c < n_chunks ? (ks0 + CHUNK_KSTAGES < kst ? ks0 + CHUNK_KSTAGES : kst) : kst + lkst;
                     for (int ks = ks0; ks < ks1; ++ks) {
                         if (*abort_flag || !mbar_wait(full_bar(stage), phase)) {
                             ok = false;
@@ -785,8 +720,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                 if (lane == 0) arrive_remote(map_to_rank(acce_bar(buf), 0));
             }
             if (!ok) break;
-            store_tile_rows<kRawInt32, kAct>(p, &tmY, out_smem, store_iter, mt * 2 * BMC + static_cast<int64_t>(rank) * BMC + q * 32,
-                                       nt * BNP + h * 128, acc, lane, h == 0 ? 128 : BNP - 128);
+            if constexpr (kLora) {
+                const uint32_t buf = chunk_iter & 1u;
+                if (*abort_flag || !mbar_wait(accf_bar(buf), (chunk_iter >> 1) & 1u)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                // the LoRA chunk stays in tensor memory until the store reads it box by box
+                store_tile_rows<kRawInt32, kAct, true>(
+                    p, &tmY, out_smem, store_iter, mt * 2 * BMC + static_cast<int64_t>(rank) * BMC + q * 32,
+                    nt * BNP + h * 128, acc, lane, h == 0 ? 128 : BNP - 128, tmem_base + lane_off + buf * BNP + h * 128);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) arrive_remote(map_to_rank(acce_bar(buf), 0));
+                ++chunk_iter;
+            } else {
+                store_tile_rows<kRawInt32, kAct>(p, &tmY, out_smem, store_iter,
+                                                 mt * 2 * BMC + static_cast<int64_t>(rank) * BMC + q * 32,
+                                                 nt * BNP + h * 128, acc, lane, h == 0 ? 128 : BNP - 128);
+            }
         }
         drain_stores(lane);
         if (!ok) fail();
@@ -802,21 +755,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 }
 
 }  // namespace pair
-
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
-{
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    });
-    return fn;
-}
 
 // 2-D map over a [rows, ld] bf16 matrix, box = box_rows x 64 elements, 128-byte swizzle.
 bool make_map(CUtensorMap *map, const void *base, int64_t rows, int64_t kpad, int64_t ld, uint32_t box_rows)
@@ -846,34 +784,40 @@ bool make_out_map(CUtensorMap *map, void *base, int64_t m, int64_t n, int64_t ld
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int sm_count()
-{
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    return n;
-}
-
 template <int BN>
-cudaError_t launch_pair(const GemmArgs &g, const TcParams &p, const CUtensorMap &ty, int sms, cudaStream_t stream)
+cudaError_t launch_pair(const GemmArgs &g, TcParams p, const CUtensorMap &ty, int sms, cudaStream_t stream)
 {
     using C = pair::Cfg<BN>;
-    CUtensorMap pa, pb;
+    CUtensorMap pa, pb, la, lb;
     if (!make_map(&pa, g.qx, g.m, g.kpad, g.ldqx, pair::BMC) || !make_map(&pb, g.qw, g.n, g.kpad, g.ldqw, C::BNC))
         return cudaErrorInvalidValue;
+    la = pa;
+    lb = pb;
+    if (g.lora_r > 0) {
+        const int lcols = lora_cols(g.lora_r);
+        if (!make_map(&la, g.lora_t, g.m, lcols, g.lora_ldt, pair::BMC) ||
+            !make_map(&lb, g.lora_b, g.n, lcols, g.lora_ldb, C::BNC))
+            return cudaErrorInvalidValue;
+        p.lora_kst = lcols / BK;
+    }
     const int64_t tiles = ((g.m + 2 * pair::BMC - 1) / (2 * pair::BMC)) * ((g.n + BN - 1) / BN);
     const int64_t pairs = tiles < sms / 2 ? tiles : sms / 2;
     const unsigned grid = static_cast<unsigned>(2 * pairs);
     auto run = [&](auto kern) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
         if (e != cudaSuccess) return e;
-        kern<<<grid, THREADS, C::SMEM_BYTES, stream>>>(pa, pb, ty, p);
+        kern<<<grid, THREADS, C::SMEM_BYTES, stream>>>(pa, pb, ty, la, lb, p);
         return cudaGetLastError();
     };
-    if (g.a) return run(pair::gemm_tc_pair_kernel<BN, true, 0>);
-    if (p.act == 1) return run(pair::gemm_tc_pair_kernel<BN, false, 1>);
-    if (p.act == 2) return run(pair::gemm_tc_pair_kernel<BN, false, 2>);
-    return run(pair::gemm_tc_pair_kernel<BN, false, 0>);
+    if (g.a) return run(pair::gemm_tc_pair_kernel<BN, true, 0, false>);
+    if (g.lora_r > 0) {
+        if (p.act == 1) return run(pair::gemm_tc_pair_kernel<BN, false, 1, true>);
+        if (p.act == 2) return run(pair::gemm_tc_pair_kernel<BN, false, 2, true>);
+        return run(pair::gemm_tc_pair_kernel<BN, false, 0, true>);
+    }
+    if (p.act == 1) return run(pair::gemm_tc_pair_kernel<BN, false, 1, false>);
+    if (p.act == 2) return run(pair::gemm_tc_pair_kernel<BN, false, 2, false>);
+    return run(pair::gemm_tc_pair_kernel<BN, false, 0, false>);
 }
 
 }  // namespace
@@ -902,7 +846,7 @@ cudaError_t launch_gemm_tc(const GemmArgs &g, cudaStream_t stream)
     p.vec_cols = (reinterpret_cast<uintptr_t>(g.sw) % 16 == 0) && (reinterpret_cast<uintptr_t>(g.bias) % 16 == 0);
     const int sms = sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
-    if (g.m > BM) {
+    if (g.m > BM || g.lora_r > 0) {  // (the LoRA chunk exists in the pair kernel only)
         // CTA pairs on 256 x 256 tiles. (224-wide tiles fill the last wave better on
         // paper but measured no faster on the DiT shapes: each chunk already runs at
         // close to the tensor peak and per-tile costs do not shrink with the width.)

@@ -39,7 +39,22 @@ struct GemmArgs {
     int64_t ldy;
     int32_t *dev_status;
     int32_t act;       // convrot_activation applied to Y (not to raw int32 output)
+    // LoRA side branch (bf16 codes only): Y += T_ext B_ext^T before the activation
+    int32_t lora_r;          // 0: none
+    const void *lora_t;      // T_ext bf16 [m, lora_ldt]
+    int64_t lora_ldt;
+    const void *lora_b;      // B_ext bf16 [n, lora_ldb]
+    int64_t lora_ldb;
 };
+
+// K extent of the LoRA chunk: 3 r rounded up to 64.
+int lora_cols(int r);
+cudaError_t launch_lora_prepare(const float *B, int64_t n, int32_t r, int64_t ldb, float scale, void *out,
+                                int64_t lde, cudaStream_t stream);
+cudaError_t launch_lora_prepare_down(const float *A, int32_t r, int32_t k, int64_t lda, float *out, int64_t ldo,
+                                     cudaStream_t stream);
+cudaError_t launch_lora_down(const float *X, int64_t m, int32_t k, int64_t ldx, const float *A_ext, int32_t r,
+                             int64_t lda, void *t, int64_t ldt, int32_t *dev_status, cudaStream_t stream);
 
 // GELU, erf or tanh form (convrot_activation), on the epilogue's fp32 value.
 __device__ __forceinline__ float apply_act(float v, int act)

@@ -1,0 +1,476 @@
+// Runtime LoRA side branch for the convrot linear.
+//
+// The page "INT8 Convrot Safetensors" (stable-diffusion.cpp docs), section
+// "Backend support", paragraph on adapters: they are applied at runtime, the
+// INT8 weights stay untouched, the convrot path gives the base output, and
+// the adapter computes its correction from the original, unrotated
+// activation and adds it to that output. For a LoRA with down matrix A
+// [r, K], up matrix B [N, r] and scale s (alpha / r in the usual files):
+//
+//   Y = base(X) + s * (X A^T) B^T
+//
+// Two kernels here, and one extra K-chunk in the linear's GEMM:
+//
+//   lora_prepare_kernel  offline, per adapter: B_ext [N, 3r] bf16 =
+//                        [hi(sB) | lo(sB) | hi(sB)], hi/lo the two-term bf16
+//                        split (hi = bf16(v), lo = bf16(v - hi)).
+//   lora_prepare_down_kernel  offline, per adapter: A_ext [2r, K] fp32 =
+//                        [hi(A); lo(A)], hi = A with its low 13 mantissa bits
+//                        cleared (exact in TF32), lo = A - hi.
+//   lora_down_kernel     per call: T = X A^T on the tensor cores (tcgen05,
+//                        kind::tf32) with three-term TF32 splitting
+//                        (T = Xh Ah + Xh Al + Xl Ah), so T carries about fp32
+//                        accuracy; then T_ext [M, 3r] bf16 =
+//                        [hi(T) | hi(T) | lo(T)].
+//   the GEMM             T_ext B_ext^T = hi(T) hi(sB) + hi(T) lo(sB) +
+//                        lo(T) hi(sB) runs as one more chunk of the
+//                        linear's K loop, accumulated in fp32 in tensor
+//                        memory and added to the reconstructed output before
+//                        any activation.
+//
+// lora_down_kernel layout: a cluster of CTAs per 128 rows of X, each taking a
+// share of K (so that about one CTA runs per SM).
+//   warp 0      TMA producer: 32-column fp32 slices of X (128 rows) and of
+//               A_ext's hi and lo rows, 128-byte swizzled, into a ring.
+//   warp 1      TMEM (r fp32 columns) and tcgen05.mma, M = 128, N = r, K = 8.
+//   warps 2-9   split each X slice in place: hi = the value with its low 13
+//               mantissa bits cleared, lo = value - hi into a second buffer
+//               with the same layout.
+//   then        each CTA's partial T goes to its shared memory; the cluster
+//               adds the partials in rank order (distributed shared memory),
+//               each CTA for its share of the rows, and writes T_ext.
+// Every wait is bounded; one that runs out writes CONVROT_ERR_TIMEOUT to the
+// caller's status word and the CTA winds down.
+#include <cuda_bf16.h>
+
+#include "../../include/convrot.h"
+#include "internal.h"
+#include "tc_common.cuh"
+
+namespace convrot {
+namespace {
+
+using namespace tc;
+
+constexpr int LD_BM = 128;  // rows of X per cluster
+constexpr int LD_BK = 32;   // fp32 elements per slice: 128 bytes, one swizzle span
+constexpr int LD_SPLIT_WARPS = 8;
+constexpr int LD_THREADS = 64 + 32 * LD_SPLIT_WARPS;
+constexpr int LD_X_BYTES = LD_BM * LD_BK * 4;  // 16 KB
+constexpr int LD_SMEM_LIMIT = 227 * 1024;
+constexpr int LD_MAX_CLUSTER = 8;
+
+// kind::tf32: D fp32 (bit 4), A and B TF32 (format 2 at bits 7 and 10), both K-major, M = 128, N = n
+__host__ __device__ constexpr uint32_t tf32_idesc(int n)
+{
+    return (1u << 4) | (2u << 7) | (2u << 10) | (uint32_t(n >> 3) << 17) | (uint32_t(LD_BM >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ float ld_cluster_f32(uint32_t local_addr, uint32_t rank)
+{
+    uint32_t a;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(local_addr), "r"(rank));
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
+    return v;
+}
+
+struct DownParams {
+    int64_t m;
+    int32_t r;
+    int32_t kstages;      // ceil(k / 32), split over the cluster's CTAs
+    int32_t stages;       // ring depth
+    uint32_t a_bytes;     // r * 128: one slice of A (hi or lo)
+    uint32_t stage_bytes; // X hi + A hi + A lo + X lo
+    uint32_t tmem_cols;   // power of two >= max(32, r)
+    __nv_bfloat16 *t;     // T_ext [m, ldt]
+    int64_t ldt;
+    int32_t t_cols;       // columns of T_ext written: 3r, then zeros up to t_cols
+    int32_t *dev_status;
+};
+
+__device__ __forceinline__ void split_tf32(float4 &big, float4 &small)
+{
+    const uint32_t mask = 0xffffe000u;  // keep sign, exponent and the 10 mantissa bits of TF32
+    float4 hi;
+    hi.x = __uint_as_float(__float_as_uint(big.x) & mask);
+    hi.y = __uint_as_float(__float_as_uint(big.y) & mask);
+    hi.z = __uint_as_float(__float_as_uint(big.z) & mask);
+    hi.w = __uint_as_float(__float_as_uint(big.w) & mask);
+    small = make_float4(big.x - hi.x, big.y - hi.y, big.z - hi.z, big.w - hi.w);  // exact
+    big = hi;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b)
+{
+    const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t *>(&v);
+}
+
+// One CTA of a cluster: rows [128 * blockIdx.y, +128) of X, its share of the K
+// slices. The cluster's CTAs then add their partial T tiles (through
+// distributed shared memory, in rank order) and write T_ext.
+__global__ void __launch_bounds__(LD_THREADS, 1)
+    lora_down_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmA, DownParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = static_cast<uint32_t>(__cvta_generic_to_shared(smem_raw));
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *gbase = smem_raw + (base - raw);
+    const int S = p.stages;
+    const uint32_t bars = base + S * p.stage_bytes;
+    auto full_bar = [&](int s) { return bars + 8u * s; };
+    auto conv_bar = [&](int s) { return bars + 8u * (S + s); };
+    auto empty_bar = [&](int s) { return bars + 8u * (2 * S + s); };
+    const uint32_t accf_bar = bars + 8u * (3 * S);
+    const uint32_t done_bar = bars + 8u * (3 * S + 1);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + S * p.stage_bytes + 8 * (3 * S + 2));
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + S * p.stage_bytes + 8 * (3 * S + 2) + 4);
+    // stage s: [X hi | A hi | A lo | X lo]
+    auto x_big = [&](int s) { return base + s * p.stage_bytes; };
+    auto a_big = [&](int s) { return x_big(s) + LD_X_BYTES; };
+    auto a_small = [&](int s) { return a_big(s) + p.a_bytes; };
+    auto x_small = [&](int s) { return a_small(s) + p.a_bytes; };
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int row0 = static_cast<int>(blockIdx.y) * LD_BM;
+    const uint32_t rank = cluster_rank();
+    const int csize = static_cast<int>(gridDim.x);
+    const int ks_begin = static_cast<int>((static_cast<int64_t>(p.kstages) * rank) / csize);
+    const int ks_end = static_cast<int>((static_cast<int64_t>(p.kstages) * (rank + 1)) / csize);
+    const int nks = ks_end - ks_begin;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(conv_bar(s), LD_SPLIT_WARPS);
+            mbar_init(empty_bar(s), 1);
+        }
+        mbar_init(accf_bar, 1);
+        mbar_init(done_bar, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmX)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         static_cast<uint32_t>(__cvta_generic_to_shared(tmem_slot))),
+                     "r"(p.tmem_cols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    auto fail = [&]() {
+        *abort_flag = 1;
+        if (p.dev_status) atomicExch(p.dev_status, static_cast<int32_t>(CONVROT_ERR_TIMEOUT));
+    };
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int issued = 0;
+            bool ok = true;
+            for (int i = 0; i < nks; ++i) {
+                const int s = i % S;
+                const uint32_t ph = static_cast<uint32_t>(i / S) & 1u;
+                if (*abort_flag || !mbar_wait(empty_bar(s), ph ^ 1u)) {
+                    ok = false;
+                    break;
+                }
+                const int kx = (ks_begin + i) * LD_BK;
+                mbar_arrive_expect_tx(full_bar(s), LD_X_BYTES + 2u * p.a_bytes);
+                tma_load_2d(x_big(s), &tmX, kx, row0, full_bar(s));
+                tma_load_2d(a_big(s), &tmA, kx, 0, full_bar(s));       // rows 0..r-1: hi(A)
+                tma_load_2d(a_small(s), &tmA, kx, p.r, full_bar(s));   // rows r..2r-1: lo(A)
+                ++issued;
+            }
+            if (!ok) {
+                fail();
+                // the copies already issued land before shared memory goes away
+                for (int i = (issued > S ? issued - S : 0); i < issued; ++i)
+                    mbar_wait(full_bar(i % S), static_cast<uint32_t>(i / S) & 1u);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t idesc = tf32_idesc(p.r);
+            bool ok = true;
+            for (int i = 0; i < nks; ++i) {
+                const int s = i % S;
+                const uint32_t ph = static_cast<uint32_t>(i / S) & 1u;
+                if (*abort_flag || !mbar_wait(conv_bar(s), ph)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < LD_BK / 8; ++kk) {  // K = 8 TF32 = 32 bytes per instruction
+                    const uint64_t xh = smem_desc(x_big(s)) + 2u * kk, ah = smem_desc(a_big(s)) + 2u * kk;
+                    const uint64_t xl = smem_desc(x_small(s)) + 2u * kk, al = smem_desc(a_small(s)) + 2u * kk;
+                    mma_tf32(tmem_base, xh, ah, idesc, (i > 0 || kk > 0) ? 1u : 0u);
+                    mma_tf32(tmem_base, xh, al, idesc, 1u);
+                    mma_tf32(tmem_base, xl, ah, idesc, 1u);
+                }
+                mma_commit(empty_bar(s));
+            }
+            if (!ok) fail();
+            mma_commit(accf_bar);  // after every MMA issued above
+            mma_commit(done_bar);
+            mbar_wait(done_bar, 0);
+        }
+        __syncwarp();
+    } else {
+        const int tid = threadIdx.x - 64;  // 0..255
+        bool ok = true;
+        for (int i = 0; i < nks; ++i) {
+            const int s = i % S;
+            const uint32_t ph = static_cast<uint32_t>(i / S) & 1u;
+            if (*abort_flag || !mbar_wait(full_bar(s), ph)) {
+                ok = false;
+                break;
+            }
+            // the split is elementwise, so the swizzled layout does not matter: same offset in both buffers
+            float4 *xb = reinterpret_cast<float4 *>(gbase + (x_big(s) - base));
+            float4 *xs = reinterpret_cast<float4 *>(gbase + (x_small(s) - base));
+#pragma unroll
+            for (int j = 0; j < LD_X_BYTES / 16 / (32 * LD_SPLIT_WARPS); ++j) {
+                float4 v = xb[tid + 32 * LD_SPLIT_WARPS * j], l;
+                split_tf32(v, l);
+                xb[tid + 32 * LD_SPLIT_WARPS * j] = v;
+                xs[tid + 32 * LD_SPLIT_WARPS * j] = l;
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the tensor core
+            __syncwarp();
+            if (lane == 0) mbar_arrive(conv_bar(s));
+        }
+        if (!ok) fail();
+    }
+
+    // partial T (this CTA's K share) from tensor memory to shared memory, [128][r + 1] fp32
+    const int r = p.r;
+    const int pitch = r + 1;  // odd: row-per-lane writes and column reads are conflict-free
+    float *part = reinterpret_cast<float *>(gbase);
+    const uint32_t part_addr = base;
+    bool ok = true;
+    if (warp >= 2 && warp < 6) {  // four warps, one per TMEM lane quadrant
+        ok = mbar_wait(accf_bar, 0) && !*abort_flag;
+        if (ok) {
+            tc_fence_after();
+            const int q = warp & 3;
+            float *dst = part + (q * 32 + lane) * pitch;
+            for (int c0 = 0; c0 < r; c0 += 32) {
+                uint32_t v[32];
+                tmem_ld32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + c0, v);
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    if (c0 + j < r) dst[c0 + j] = __uint_as_float(v[j]);
+            }
+        } else {
+            fail();
+        }
+    }
+    tc_fence_before();
+    cluster_sync();  // every CTA's partial is in its shared memory (all CTAs reach this)
+    // this CTA adds the cluster's partials, in rank order, for its share of the rows
+    if (!*abort_flag) {
+        const int rows_per = (LD_BM + csize - 1) / csize;
+        const int rb = static_cast<int>(rank) * rows_per;
+        const int re = rb + rows_per < LD_BM ? rb + rows_per : LD_BM;
+        const int pairs = r / 2;
+        for (int idx = threadIdx.x; idx < (re - rb) * pairs; idx += LD_THREADS) {
+            const int rr = rb + idx / pairs, c = (idx % pairs) * 2;
+            const uint32_t a = part_addr + static_cast<uint32_t>((rr * pitch + c) * 4);
+            // all the remote loads first (they overlap), then the sums in rank order
+            float v0[LD_MAX_CLUSTER], v1[LD_MAX_CLUSTER];
+#pragma unroll
+            for (int src = 0; src < LD_MAX_CLUSTER; ++src) {
+                if (src < csize) {
+                    v0[src] = ld_cluster_f32(a, static_cast<uint32_t>(src));
+                    v1[src] = ld_cluster_f32(a + 4, static_cast<uint32_t>(src));
+                }
+            }
+            float t0 = 0.0f, t1 = 0.0f;
+#pragma unroll
+            for (int src = 0; src < LD_MAX_CLUSTER; ++src) {
+                if (src < csize) {
+                    t0 += v0[src];
+                    t1 += v1[src];
+                }
+            }
+            const int64_t row = static_cast<int64_t>(row0) + rr;
+            if (row >= p.m) continue;
+            const __nv_bfloat162 h = __floats2bfloat162_rn(t0, t1);
+            const float2 hf = __bfloat1622float2(h);
+            uint32_t *dst = reinterpret_cast<uint32_t *>(p.t + row * p.ldt);
+            const uint32_t hb = *reinterpret_cast<const uint32_t *>(&h);
+            dst[c / 2] = hb;
+            dst[(r + c) / 2] = hb;
+            dst[(2 * r + c) / 2] = pack_bf16x2(t0 - hf.x, t1 - hf.y);
+        }
+        // the zero columns past 3 r
+        const int zpairs = (p.t_cols - 3 * r) / 2;
+        for (int idx = threadIdx.x; idx < (re - rb) * zpairs; idx += LD_THREADS) {
+            const int64_t row = static_cast<int64_t>(row0) + rb + idx / zpairs;
+            if (row < p.m)
+                reinterpret_cast<uint32_t *>(p.t + row * p.ldt)[(3 * r) / 2 + idx % zpairs] = 0u;
+        }
+    }
+    cluster_sync();  // no CTA leaves while another may still read its partial
+    if (warp == 1)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(p.tmem_cols)
+                     : "memory");
+}
+
+// A_ext [2r, lda_ext] fp32: rows 0..r-1 = A with the low 13 mantissa bits cleared (exact in TF32),
+// rows r..2r-1 = A minus that.
+__global__ void lora_prepare_down_kernel(const float *A, int32_t r, int32_t k, int64_t lda, float *out, int64_t ldo)
+{
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i >= static_cast<int64_t>(r) * k) return;
+    const int64_t j = i / k, c = i - j * k;
+    const float v = A[j * lda + c];
+    const float hi = __uint_as_float(__float_as_uint(v) & 0xffffe000u);
+    out[j * ldo + c] = hi;
+    out[(j + r) * ldo + c] = v - hi;
+}
+
+// B_ext[o] = [hi(s B[o]) | lo(s B[o]) | hi(s B[o]) | 0 ...]: one thread per (o, pair of columns).
+__global__ void lora_prepare_kernel(const float *B, int64_t n, int32_t r, int64_t ldb, float scale,
+                                    __nv_bfloat16 *out, int64_t lde, int32_t cols)
+{
+    const int64_t per_row = cols / 2;
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i >= n * per_row) return;
+    const int64_t o = i / per_row;
+    const int c = static_cast<int>(i - o * per_row) * 2;  // even column of the output row
+    uint32_t *dst = reinterpret_cast<uint32_t *>(out + o * lde + c);
+    if (c >= 3 * r) {
+        *dst = 0u;
+        return;
+    }
+    const int part = c / r, j = c - part * r;  // r is even, so a pair never straddles two parts
+    const float v0 = scale * B[o * ldb + j], v1 = scale * B[o * ldb + j + 1];
+    const __nv_bfloat162 h = __floats2bfloat162_rn(v0, v1);
+    if (part == 1) {
+        const float2 hf = __bfloat1622float2(h);
+        *dst = pack_bf16x2(v0 - hf.x, v1 - hf.y);
+    } else {
+        *dst = *reinterpret_cast<const uint32_t *>(&h);
+    }
+}
+
+}  // namespace
+
+int lora_cols(int r) { return (3 * r + 63) / 64 * 64; }
+
+cudaError_t launch_lora_prepare(const float *B, int64_t n, int32_t r, int64_t ldb, float scale, void *out,
+                                int64_t lde, cudaStream_t stream)
+{
+    if (n == 0) return cudaSuccess;
+    const int cols = lora_cols(r);
+    const int64_t total = n * (cols / 2);
+    const int threads = 256;
+    const int64_t blocks = (total + threads - 1) / threads;
+    if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
+    lora_prepare_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
+        B, n, r, ldb, scale, static_cast<__nv_bfloat16 *>(out), lde, cols);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_lora_prepare_down(const float *A, int32_t r, int32_t k, int64_t lda, float *out, int64_t ldo,
+                                     cudaStream_t stream)
+{
+    const int64_t total = static_cast<int64_t>(r) * k;
+    const int threads = 256;
+    const int64_t blocks = (total + threads - 1) / threads;
+    if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
+    lora_prepare_down_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(A, r, k, lda, out, ldo);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_lora_down(const float *X, int64_t m, int32_t k, int64_t ldx, const float *A_ext, int32_t r,
+                             int64_t lda, void *t, int64_t ldt, int32_t *dev_status, cudaStream_t stream)
+{
+    if (m == 0) return cudaSuccess;
+    CUtensorMap mx, ma;
+    if (!make_map_2d(&mx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, X, m, k, ldx * 4, LD_BK, LD_BM) ||
+        !make_map_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, A_ext, 2 * r, k, lda * 4, LD_BK, static_cast<uint32_t>(r)))
+        return cudaErrorInvalidValue;
+    DownParams p{};
+    p.m = m;
+    p.r = r;
+    p.kstages = (k + LD_BK - 1) / LD_BK;
+    p.a_bytes = static_cast<uint32_t>(r) * LD_BK * 4;
+    p.stage_bytes = 2u * (LD_X_BYTES + p.a_bytes);
+    const int fixed = 1024 + 256;  // alignment slack, barriers, TMEM slot and flag
+    int stages = (LD_SMEM_LIMIT - fixed) / static_cast<int>(p.stage_bytes);
+    stages = stages > 4 ? 4 : stages;
+    if (stages < 2) return cudaErrorInvalidValue;
+    // the partial-T tile [128][r + 1] fp32 reuses the ring once the K loop is done
+    if (static_cast<int64_t>(LD_BM) * (r + 1) * 4 > static_cast<int64_t>(stages) * p.stage_bytes)
+        return cudaErrorInvalidValue;
+    p.stages = stages;
+    uint32_t cols = 32;
+    while (cols < static_cast<uint32_t>(r)) cols <<= 1;
+    p.tmem_cols = cols;
+    p.t = static_cast<__nv_bfloat16 *>(t);
+    p.ldt = ldt;
+    p.t_cols = lora_cols(r);
+    p.dev_status = dev_status;
+    const int smem = fixed + stages * static_cast<int>(p.stage_bytes);
+    cudaError_t e = cudaFuncSetAttribute(lora_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    const int64_t row_blocks = (m + LD_BM - 1) / LD_BM;
+    if (row_blocks > 65535) return cudaErrorInvalidConfiguration;
+    // split K over a cluster so that about one CTA runs per SM
+    int sms = sm_count();
+    if (sms <= 0) return cudaErrorInvalidDevice;
+    int cs = static_cast<int>(sms / row_blocks);
+    cs = cs < 1 ? 1 : (cs > LD_MAX_CLUSTER ? LD_MAX_CLUSTER : cs);
+    if (cs > p.kstages) cs = p.kstages;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(cs), static_cast<unsigned>(row_blocks), 1);
+    cfg.blockDim = dim3(LD_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(cs);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, lora_down_kernel, mx, ma, p);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+}  // namespace convrot

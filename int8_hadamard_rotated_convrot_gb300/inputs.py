@@ -40,6 +40,8 @@ class Workload:
     linears: int = 1  # linears sharing one packed X (q, k, v -> 3)
     act: int = 0      # activation after the (first) linear: 0 none, 1 GELU erf form, 2 GELU tanh form
     down_n: int = 0   # > 0: a DiT MLP pair; the activated output feeds a down projection to down_n features
+    lora_r: int = 0   # > 0: a runtime LoRA of this rank on the (first) linear
+    lora_scale: float = 2.0  # alpha / r
     notes: str = field(default="", compare=False)
 
     @property
@@ -49,7 +51,9 @@ class Workload:
 
     @property
     def step_ops(self) -> int:
-        """2*M*N*K summed over every GEMM of one step (all linears, both MLP projections)."""
+        """2*M*N*K summed over every GEMM of one step (all linears, both MLP projections).
+        A LoRA's own multiply-adds (2 M r (K + N)) are not counted: the metric is the
+        convrot linear's."""
         return sum(2 * self.m * st.n * st.k for st in stage_shapes(self))
 
     @property
@@ -129,6 +133,17 @@ def stage_weights(wl: Workload, s: int):
     return [weights(wl, i) for i in range(count)], np.concatenate([bias(wl, i) for i in range(count)])
 
 
+_LORA_A, _LORA_B = 20, 21  # substream indices of the adapter's matrices
+
+
+def lora_weights(wl: Workload):
+    """(A [r, k], B [n, r]) fp32 of the workload's adapter, both ~ N(0, 0.02^2)."""
+    r, n = wl.lora_r, wl.n * wl.linears
+    A = np.random.default_rng(list(wl.seed) + [_TAG_W, _LORA_A]).standard_normal((r, wl.k), dtype=np.float32)
+    B = np.random.default_rng(list(wl.seed) + [_TAG_W, _LORA_B]).standard_normal((n, r), dtype=np.float32)
+    return A * np.float32(0.02), B * np.float32(0.02)
+
+
 def _sweep(G: int) -> Workload:
     return Workload(f"sweep_G{G}", 4096, 3072, 3072, G, (3, G))
 
@@ -140,6 +155,8 @@ WORKLOADS = {
         Workload("attn_qkv", 4096, 3072, 3072, 256, (1,), linears=3),
         Workload("mlp_up", 4096, 3072, 12288, 256, (2, 0)),
         Workload("mlp_down", 4096, 12288, 3072, 256, (2, 1), gelu_input=True),
+        Workload("mlp_up_lora", 4096, 3072, 12288, 256, (2, 0), lora_r=64, lora_scale=2.0,
+                 notes="MLP up with a rank-64 runtime LoRA, scale 128/64 (the rank and alpha of the page's example)"),
         Workload("mlp_pair", 4096, 3072, 12288, 256, (2, 2), act=1, down_n=3072,
                  notes="up projection with GELU fused in its epilogue, then pack + down projection"),
         *[_sweep(G) for G in (4, 16, 64, 256, 1024)],

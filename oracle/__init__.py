@@ -70,6 +70,8 @@ def _load():
         lib.oracle_reconstruct.restype = None
         lib.oracle_pack_rows.argtypes = [vp, i64, i64, i64, i64, vp, vp, i64, vp]
         lib.oracle_pack_rows.restype = ctypes.c_int
+        lib.oracle_lora_delta.argtypes = [vp, i64, i64, i64, vp, i64, vp, i64, ctypes.c_double, vp, vp]
+        lib.oracle_lora_delta.restype = None
         lib.oracle_activation.argtypes = [vp, i64, ctypes.c_int]
         lib.oracle_activation.restype = None
         lib.oracle_num_threads.argtypes = []
@@ -195,8 +197,27 @@ def activation(v: np.ndarray, act: int) -> np.ndarray:
     return out
 
 
-def reconstruct(A: np.ndarray, sx: np.ndarray, sw: np.ndarray, bias: np.ndarray | None, act: int = 0):
-    """Y = act(A * s_x[r] * s_w[o] + b[o]) in fp64; returns (Y fp32, Y fp64)."""
+def lora_delta(X: np.ndarray, A: np.ndarray, B: np.ndarray, scale: float):
+    """(T = X A^T, D = scale * T B^T), both fp64, from the unrotated X (r <= 256)."""
+    X = _rows_f32(X)
+    A = np.ascontiguousarray(A, dtype=np.float32)
+    B = np.ascontiguousarray(B, dtype=np.float32)
+    m, k = X.shape
+    r = A.shape[0]
+    n = B.shape[0]
+    if A.shape[1] != k or B.shape[1] != r or r > 256:
+        raise ValueError("shapes: X [m, k], A [r, k], B [n, r], r <= 256")
+    T = np.empty((m, r), np.float64)
+    D = np.empty((m, n), np.float64)
+    _load().oracle_lora_delta(_ptr(X), m, k, X.strides[0] // 4, _ptr(A), r, _ptr(B), n, float(scale), _ptr(T),
+                              _ptr(D))
+    return T, D
+
+
+def reconstruct(A: np.ndarray, sx: np.ndarray, sw: np.ndarray, bias: np.ndarray | None, act: int = 0,
+                add: np.ndarray | None = None):
+    """Y = act(A * s_x[r] * s_w[o] + b[o] + add[r, o]) in fp64 (add: e.g. a LoRA
+    correction, added before the activation); returns (Y fp32, Y fp64)."""
     A = np.ascontiguousarray(A, dtype=np.int32)
     sx = np.ascontiguousarray(sx, dtype=np.float32)
     sw = np.ascontiguousarray(sw, dtype=np.float32)
@@ -206,8 +227,11 @@ def reconstruct(A: np.ndarray, sx: np.ndarray, sw: np.ndarray, bias: np.ndarray 
     Y64 = np.empty((m, n), np.float64)
     _load().oracle_reconstruct(_ptr(A), n, m, n, _ptr(sx), _ptr(sw), _ptr(b), _ptr(Y), n,
                                _ptr(Y64))
+    if add is not None:
+        Y64 = Y64 + np.asarray(add, np.float64)
     if act:
         Y64 = activation(Y64, act)
+    if add is not None or act:
         Y = Y64.astype(np.float32)
     return Y, Y64
 

@@ -272,6 +272,32 @@ void oracle_activation(double *v, int64_t count, int act)
 }
 
 /*
+ * Runtime LoRA correction ("Backend support", paragraph on adapters): from the
+ * original, unrotated activation, D = scale * (X A^T) B^T, with A [r, k]
+ * (down) and B [n, r] (up), in fp64. T [m, r] receives X A^T (may be NULL).
+ * D is [m, n] with row pitch n.
+ */
+void oracle_lora_delta(const float *X, int64_t m, int64_t k, int64_t ldx, const float *A, int64_t r,
+                       const float *B, int64_t n, double scale, double *T, double *D)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < m; i++) {
+        double t[256];
+        double *ti = T ? T + i * r : t;
+        for (int64_t j = 0; j < r; j++) {
+            double acc = 0.0;
+            for (int64_t c = 0; c < k; c++) acc += (double)X[i * ldx + c] * (double)A[j * k + c];
+            ti[j] = acc;
+        }
+        for (int64_t o = 0; o < n; o++) {
+            double acc = 0.0;
+            for (int64_t j = 0; j < r; j++) acc += ti[j] * (double)B[o * r + j];
+            D[i * n + o] = scale * acc;
+        }
+    }
+}
+
+/*
  * Whole pack of rows: rotate (fast form) then quantize. Used for the
  * activation pack and for the offline weight quantization, which the page
  * defines with the same formulas. Q is int8 [m, ldq]; columns k..ldq-1 are

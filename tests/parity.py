@@ -91,3 +91,51 @@ def check_y_end_to_end(y_gpu: np.ndarray, y_ref: np.ndarray, qx=None, qw=None, s
                                           * (fx[:, None] + fw[None, :]))
     bad = err > tol
     assert not bad.any(), f"{bad.sum()} outputs off end to end; worst |dY| = {err.max():.3e}, 1e-3 * max|Y| = {Y_END_TO_END * ref:.3e}"
+
+
+def lora_t_tolerance(k: int) -> float:
+    """Relative bound (to sum_i |X_i||A_i|) on T = X A^T from three-term TF32:
+    every product is formed exactly from the split parts except the dropped
+    lo*lo term and lo's own TF32 rounding (together < 2^-20), and the sum
+    runs over 3k terms in fp32 with at most one ulp (2^-23) lost per add."""
+    return 3 * k * 2.0 ** -23 + 2.0 ** -20
+
+
+def lora_t_rms_tolerance(k: int) -> float:
+    """Typical size of the same error: independent roundings over 3k adds grow
+    like sqrt(3k) * 2^-24; four of those."""
+    return 4 * math.sqrt(3 * k) * 2.0 ** -24
+
+
+def check_lora_t(t_gpu, t_ref, l1, k):
+    """T against the fp64 oracle; l1 = |X| |A|^T."""
+    err = np.abs(np.asarray(t_gpu, np.float64) - t_ref)
+    tol = lora_t_tolerance(k) * l1 + 2.0 ** -17 * np.abs(t_ref) + 1e-30  # + the bf16 hi/lo form of T
+    assert not (err > tol).any(), f"{(err > tol).sum()} of T off; worst {np.max(err / tol):.3e} of the tolerance"
+    rms = math.sqrt(float(np.mean(err ** 2)))
+    rms_l1 = math.sqrt(float(np.mean(l1 ** 2)))
+    assert rms <= lora_t_rms_tolerance(k) * rms_l1 + 2.0 ** -17 * math.sqrt(float(np.mean(t_ref ** 2))), \
+        f"rms error {rms:.3e} vs {lora_t_rms_tolerance(k) * rms_l1:.3e}"
+
+
+def check_y_lora_same_codes(y_gpu, y64_ref, A, sx, sw, bias, lora_l1, k, r, act):
+    """Y = act(base + D): the base rule (1e-6 of |A s_x s_w| + |b|), plus for the
+    correction D (magnitude lora_l1 = scale |X| |A|^T |B|^T) the T bound, the
+    two-term bf16 split of T and of scale*B (2^-15) and the fp32 sum over
+    3r terms (3r * 2^-23); times GELU's largest slope 1.13 when act, plus 3e-7 |Y|."""
+    base = np.abs(A.astype(np.float64) * np.asarray(sx, np.float64)[:, None] * np.asarray(sw, np.float64)[None, :])
+    if bias is not None:
+        base = base + np.abs(np.asarray(bias, np.float64))[None, :]
+    c = lora_t_tolerance(k) + 2.0 ** -15 + 3 * r * 2.0 ** -23
+    tol = 1e-6 * base + c * lora_l1
+    if act:
+        tol = 1.13 * tol + 3e-7 * np.abs(y64_ref)
+    tol = tol + 1e-30
+    err = np.abs(np.asarray(y_gpu, np.float64) - y64_ref)
+    bad = err > tol
+    assert not bad.any(), f"{bad.sum()} outputs off; worst {np.max(err / tol):.3e} of the tolerance"
+    # typical size: a dropped hi/lo term (2^-9 relative) would stand far above this
+    rms = lambda a: math.sqrt(float(np.mean(np.square(a))))
+    typ = (lora_t_rms_tolerance(k) + 2.0 ** -15 + 4 * math.sqrt(3 * r) * 2.0 ** -24) * rms(lora_l1) + 1e-6 * rms(base)
+    assert rms(err) <= (1.13 if act else 1.0) * typ + (3e-7 * rms(y64_ref) if act else 0.0), \
+        f"rms error {rms(err):.3e} above the typical bound {typ:.3e}"

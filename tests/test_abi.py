@@ -157,3 +157,41 @@ def test_linear_act_rejects_unknown_activation(lib):
             cr.ERR_INVALID_ARG
     x, w = pair(mx=0)
     assert lib.convrot_linear_act(ctypes.byref(x), ctypes.byref(w), None, cr.ACT_GELU_ERF, None, 64, None, None) == cr.OK
+
+
+def test_lora_cols(lib):
+    assert lib.convrot_lora_cols(16) == 64
+    assert lib.convrot_lora_cols(64) == 192
+    assert lib.convrot_lora_cols(48) == 192
+    assert lib.convrot_lora_cols(256) == 768
+    for r in (0, 8, 24, 272, -16):
+        assert lib.convrot_lora_cols(r) == 0
+
+
+def test_lora_entry_points_validate(lib):
+    assert lib.convrot_lora_prepare(FAKE, 4, 24, 24, 1.0, FAKE, 128, None) == cr.ERR_INVALID_ARG  # r % 16
+    assert lib.convrot_lora_prepare(FAKE, 4, 16, 8, 1.0, FAKE, 64, None) == cr.ERR_INVALID_ARG   # ldb < r
+    assert lib.convrot_lora_prepare(FAKE, 4, 16, 16, 1.0, FAKE, 32, None) == cr.ERR_INVALID_ARG  # lde < cols
+    assert lib.convrot_lora_prepare(FAKE, 4, 16, 16, 1.0, FAKE + 8, 64, None) == cr.ERR_ALIGNMENT
+    assert lib.convrot_lora_prepare(None, 0, 16, 16, 1.0, None, 64, None) == cr.OK
+    assert lib.convrot_lora_down(FAKE, 4, 0, 256, FAKE, 16, 256, FAKE, 64, None, None) == cr.ERR_K_RANGE
+    assert lib.convrot_lora_down(FAKE, 4, 256, 250, FAKE, 16, 256, FAKE, 64, None, None) == cr.ERR_INVALID_ARG
+    assert lib.convrot_lora_down(FAKE + 4, 4, 256, 256, FAKE, 16, 256, FAKE, 64, None, None) == cr.ERR_ALIGNMENT
+    assert lib.convrot_lora_down(FAKE, 4, 256, 256, FAKE, 16, 256, FAKE, 60, None, None) == cr.ERR_INVALID_ARG
+    assert lib.convrot_lora_down(None, 0, 256, 256, None, 16, 256, None, 64, None, None) == cr.OK
+    assert lib.convrot_lora_prepare_down(FAKE, 16, 0, 256, FAKE, 256, None) == cr.ERR_K_RANGE
+    assert lib.convrot_lora_prepare_down(FAKE, 16, 256, 256, FAKE + 4, 256, None) == cr.ERR_ALIGNMENT
+    assert lib.convrot_lora_prepare_down(FAKE, 12, 256, 256, FAKE, 256, None) == cr.ERR_INVALID_ARG
+
+
+def test_linear_lora_validates(lib):
+    x, w = pair(codes=cr.CODES_BF16)
+    call = lambda x, w, r=16, t=FAKE, ldt=64, b=FAKE, ldb=64: lib.convrot_linear_lora(
+        ctypes.byref(x), ctypes.byref(w), None, 0, t, ldt, b, ldb, r, FAKE, 64, None, None)
+    assert call(x, w, r=0) == cr.ERR_INVALID_ARG
+    assert call(x, w, r=20) == cr.ERR_INVALID_ARG
+    assert call(x, w, ldt=32) == cr.ERR_INVALID_ARG
+    assert call(x, w, t=FAKE + 8) == cr.ERR_ALIGNMENT
+    assert call(x, w, t=None) == cr.ERR_INVALID_ARG
+    xi, wi = pair(codes=cr.CODES_I8)
+    assert call(xi, wi) == cr.ERR_UNSUPPORTED

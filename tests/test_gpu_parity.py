@@ -378,3 +378,72 @@ def test_full_size_attention_grouped_qkv():
     _, Y64 = oracle.reconstruct(A_ref, sx_ref, sw_ref, np.concatenate(bs))
     parity.check_y_end_to_end(Y[torch.from_numpy(rows).cuda()].cpu().numpy(), Y64, (codes_np(px)[rows], Qx_ref),
                               (codes_np(pw), Qw_ref), px.scale.cpu().numpy()[rows], pw.scale.cpu().numpy())
+
+
+# ---- runtime LoRA side branch
+
+@pytest.mark.parametrize("m,k,r", [(300, 512, 16), (129, 3072, 64), (64, 200, 48), (1000, 1024, 256)])
+def test_lora_down_against_oracle(m, k, r):
+    """T = X A^T (three-term TF32 on tcgen05), stored as [hi | hi | lo | 0]."""
+    rng = np.random.default_rng(m + k + r)
+    X = special_rows(rng, m, k)
+    A = (0.05 * rng.standard_normal((r, k))).astype(np.float32)
+    cols = cr.lora_cols(r)
+    Tbig = torch.full((m + 1, cols + 8), 7.0, dtype=torch.bfloat16, device="cuda")  # canaries
+    A_ext = cr.convrot_lora_prepare_down(to_dev(A))
+    ah, al = A_ext[:r, :k].cpu().numpy(), A_ext[r:, :k].cpu().numpy()
+    np.testing.assert_array_equal(ah.astype(np.float64) + al, A.astype(np.float64))  # the split is exact
+    assert np.all((ah.view(np.uint32) & 0x1fff) == 0)
+    T_ext = cr.convrot_lora_down(to_dev(X), A_ext, out=Tbig[:m, :cols])
+    torch.cuda.synchronize()
+    t = T_ext.float().cpu().numpy()
+    assert torch.all(Tbig[m:] == 7.0) and torch.all(Tbig[:, cols:] == 7.0)
+    np.testing.assert_array_equal(t[:, :r], t[:, r:2 * r])
+    assert np.all(t[:, 3 * r:] == 0.0)
+    T_ref, _ = oracle.lora_delta(X, A, np.zeros((1, r), np.float32), 1.0)
+    l1 = np.abs(X.astype(np.float64)) @ np.abs(A.astype(np.float64)).T
+    parity.check_lora_t(t[:, :r].astype(np.float64) + t[:, 2 * r:3 * r], T_ref, l1, k)
+
+
+@pytest.mark.parametrize("m,n,k,r,act", [(300, 300, 512, 32, 0), (300, 512, 1024, 64, 1), (64, 1000, 256, 16, 2),
+                                         (513, 256, 3072, 128, 0)])
+def test_linear_lora_identical_codes(m, n, k, r, act):
+    """Y = act(A s_x s_w + b + scale (X A_l^T) B_l^T) with the LoRA term as an extra
+    fp32 chunk of the pair GEMM (also for m <= 128)."""
+    rng = np.random.default_rng(m * 3 + n + k + r)
+    X = special_rows(rng, m, k)
+    Qx, Qw = random_codes(rng, m, k), random_codes(rng, n, k)
+    sx = rng.uniform(0.0001, 0.002, m).astype(np.float32)
+    sw = rng.uniform(0.0001, 0.002, n).astype(np.float32)
+    b = rng.standard_normal(n).astype(np.float32)
+    Al = (0.05 * rng.standard_normal((r, k))).astype(np.float32)
+    Bl = (0.05 * rng.standard_normal((n, r))).astype(np.float32)
+    scale = 2.0
+    px = cr.packed_from_codes(to_dev(Qx), to_dev(sx), 64, cr.CODES_BF16)
+    pw = cr.packed_from_codes(to_dev(Qw), to_dev(sw), 64, cr.CODES_BF16)
+    T_ext = cr.convrot_lora_down(to_dev(X), cr.convrot_lora_prepare_down(to_dev(Al)))
+    B_ext = cr.convrot_lora_prepare(to_dev(Bl), scale)
+    Ybig = torch.full((m + 1, (n + 7) // 4 * 4), -3.0, dtype=torch.float32, device="cuda")
+    Y = cr.convrot_linear_lora(px, pw, to_dev(b), act, T_ext, B_ext, r, out=Ybig[:m, :n])
+    torch.cuda.synchronize()
+    assert torch.all(Ybig[m:] == -3.0) and torch.all(Ybig[:, n:] == -3.0)
+    A_ref = oracle.gemm_i32(Qx, Qw, k)
+    _, D = oracle.lora_delta(X, Al, Bl, scale)
+    _, Y64 = oracle.reconstruct(A_ref, sx, sw, b, act, add=D)
+    l1 = scale * (np.abs(X.astype(np.float64)) @ np.abs(Al.astype(np.float64)).T) @ np.abs(Bl.astype(np.float64)).T
+    parity.check_y_lora_same_codes(Y.cpu().numpy(), Y64, A_ref, sx, sw, b, l1, k, r, act)
+    # the correction is not negligible next to the base output
+    assert np.abs(D).mean() > 0.05 * np.abs(Y64).mean()
+
+
+def test_lora_prepare_layout():
+    rng = np.random.default_rng(9)
+    n, r = 70, 48
+    Bl = rng.standard_normal((n, r)).astype(np.float32)
+    ext = cr.convrot_lora_prepare(to_dev(Bl), 1.5).float().cpu().numpy()
+    v = 1.5 * Bl.astype(np.float64)
+    hi, lo = ext[:, :r], ext[:, r:2 * r]
+    np.testing.assert_array_equal(ext[:, 2 * r:3 * r], hi)
+    assert np.all(ext[:, 3 * r:] == 0.0)
+    assert np.all(np.abs(hi - v) <= 2.0 ** -8 * np.abs(v))          # hi is v rounded to bf16
+    assert np.all(np.abs(hi + lo - v) <= 2.0 ** -16 * np.abs(v))    # hi + lo carries ~16 bits

@@ -313,3 +313,43 @@ def test_linear_with_activation_is_activation_of_linear():
         got = oracle.linear(X, W, b, 16, act=act)
         np.testing.assert_array_equal(got["A"], base["A"])
         np.testing.assert_allclose(got["Y64"], oracle.activation(base["Y64"], act), rtol=0, atol=0)
+
+
+# ---- runtime LoRA correction (page: "Backend support", paragraph on adapters)
+
+def test_lora_delta_rank_one_by_hand():
+    """A = e_i (one row), B = e_j (one column): the correction is scale * X[:, i] in column j."""
+    rng = np.random.default_rng(51)
+    X = rng.standard_normal((6, 20)).astype(np.float32)
+    A = np.zeros((1, 20), np.float32)
+    A[0, 7] = 1.0
+    B = np.zeros((5, 1), np.float32)
+    B[3, 0] = 1.0
+    T, D = oracle.lora_delta(X, A, B, 2.5)
+    np.testing.assert_array_equal(T[:, 0], X[:, 7].astype(np.float64))
+    expect = np.zeros((6, 5))
+    expect[:, 3] = 2.5 * X[:, 7].astype(np.float64)
+    np.testing.assert_array_equal(D, expect)
+
+
+def test_lora_delta_is_the_merged_weight_update():
+    """(X A^T) B^T = X (B A)^T: the correction equals what merging s B A into W
+    would add, computed here in the other association order."""
+    rng = np.random.default_rng(52)
+    X = rng.standard_normal((9, 64)).astype(np.float32)
+    A = rng.standard_normal((16, 64)).astype(np.float32)
+    B = rng.standard_normal((11, 16)).astype(np.float32)
+    _, D = oracle.lora_delta(X, A, B, 0.75)
+    merged = X.astype(np.float64) @ (0.75 * (B.astype(np.float64) @ A.astype(np.float64))).T
+    np.testing.assert_allclose(D, merged, rtol=1e-12, atol=1e-12)
+
+
+def test_lora_correction_enters_before_the_activation():
+    rng = np.random.default_rng(53)
+    A_int = rng.integers(-1000, 1000, size=(4, 6)).astype(np.int32)
+    sx = rng.uniform(0.01, 0.1, 4).astype(np.float32)
+    sw = rng.uniform(0.01, 0.1, 6).astype(np.float32)
+    add = rng.standard_normal((4, 6))
+    _, plain = oracle.reconstruct(A_int, sx, sw, None)
+    _, with_add = oracle.reconstruct(A_int, sx, sw, None, act=1, add=add)
+    np.testing.assert_allclose(with_add, oracle.activation(plain + add, 1), rtol=0, atol=0)
