@@ -75,6 +75,26 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b
         : "memory");
 }
 
+// Tile order: bands of kGroupM row blocks, N-fastest inside a band, so that
+// the tiles in flight at once (one per CTA or pair) share a few A panels and a
+// few B panels that stay in L2. (With M-fastest order on M = 32760 the tiles in
+// flight spanned 76 A panels, more than L2, and A streamed from HBM once per
+// column of tiles.) For M <= kGroupM row blocks this is the plain M-fastest order.
+constexpr int64_t kGroupM = 16;
+
+__device__ __forceinline__ void tile_coords(int64_t t64, int64_t n_mt64, int64_t n_nt64, int64_t &mt, int64_t &nt)
+{
+    // (tile counts stay far below 2^31: 32-bit arithmetic)
+    const uint32_t t = static_cast<uint32_t>(t64), n_mt = static_cast<uint32_t>(n_mt64);
+    const uint32_t per_band = static_cast<uint32_t>(kGroupM) * static_cast<uint32_t>(n_nt64);
+    const uint32_t band = t / per_band;
+    const uint32_t first = band * static_cast<uint32_t>(kGroupM);
+    const uint32_t rows = n_mt - first < static_cast<uint32_t>(kGroupM) ? n_mt - first : static_cast<uint32_t>(kGroupM);
+    const uint32_t local = t - band * per_band;
+    mt = first + local % rows;
+    nt = local / rows;
+}
+
 struct TcParams {
     int64_t m, n;
     int32_t vec_cols;  // s_w and bias are 16-byte aligned
@@ -306,7 +326,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             int issued = 0;
             bool ok = true;
             for (int64_t t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
-                const int mt = static_cast<int>(t % n_mt), nt = static_cast<int>(t / n_mt);
+                int64_t mt64, nt64;
+                tile_coords(t, n_mt, n_nt, mt64, nt64);
+                const int mt = static_cast<int>(mt64), nt = static_cast<int>(nt64);
                 for (int ks = 0; ks < kst; ++ks) {
                     if (*abort_flag || !mbar_wait(empty_bar(stage), phase ^ 1u)) {
                         ok = false;
@@ -391,7 +413,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         uint32_t chunk_iter = 0;
         bool ok = true;
         for (int64_t t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
-            const int64_t mt = t % n_mt, nt = t / n_mt;
+            int64_t mt, nt;
+            tile_coords(t, n_mt, n_nt, mt, nt);
             int32_t acc[128];
 #pragma unroll
             for (int i = 0; i < 128; ++i) acc[i] = 0;
@@ -605,7 +628,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             int issued = 0;
             bool ok = true;
             for (int64_t t = pair_id; t < n_tiles && ok; t += n_pairs) {
-                const int mt = static_cast<int>(t % n_mt), nt = static_cast<int>(t / n_mt);
+                int64_t mt64, nt64;
+                tile_coords(t, n_mt, n_nt, mt64, nt64);
+                const int mt = static_cast<int>(mt64), nt = static_cast<int>(nt64);
                 const int arow = mt * 2 * BMC + static_cast<int>(rank) * BMC;
                 const int brow = nt * BNP + static_cast<int>(rank) * BNC;
                 for (int ks = 0; ks < kst + lkst; ++ks) {
@@ -695,7 +720,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         uint32_t chunk_iter = 0;
         bool ok = true;
         for (int64_t t = pair_id; t < n_tiles && ok; t += n_pairs) {
-            const int64_t mt = t % n_mt, nt = t / n_mt;
+            int64_t mt, nt;
+            tile_coords(t, n_mt, n_nt, mt, nt);
             int32_t acc[128];
 #pragma unroll
             for (int i = 0; i < 128; ++i) acc[i] = 0;
