@@ -354,24 +354,47 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
     clk = clocks.stop()
 
-    # end to end through the public API: pinned host X in, pinned host Y out, every step
-    e2e_steps = max(3, min(args.steps, 10))
+    # end to end through the public API: every step copies its X from pinned host memory
+    # and its Y back to pinned host memory. Steps are pipelined as a throughput user would:
+    # step i's Y goes to the host on one copy stream while step i+1's X comes in on another
+    # and step i+1 computes; two device and two host buffer sets alternate.
+    e2e_steps = max(4, min(args.steps, 10))
     Xh = torch.from_numpy(inputs.activations(wl)).pin_memory()
-    Yh = torch.empty((wl.m, n_out), dtype=torch.float32).pin_memory()
-    Xd = torch.empty_like(Xs[0])
+    Yh = [torch.empty((wl.m, n_out), dtype=torch.float32).pin_memory() for _ in range(2)]
+    Xd = [torch.empty_like(Xs[0]) for _ in range(2)]
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]   # compute of the set finished
+    ev_out = [torch.cuda.Event() for _ in range(2)]    # its Y is on the host
+    for e in ev_done + ev_out:
+        e.record(stream)
 
-    def e2e_step():
-        Xd.copy_(Xh, non_blocking=True)
-        Yh.copy_(run_stages(Xd, 0), non_blocking=True)
+    def e2e_step(i):
+        j = i % 2
+        with torch.cuda.stream(s_in):
+            s_in.wait_event(ev_done[j])          # the set's previous X is no longer read
+            Xd[j].copy_(Xh, non_blocking=True)
+            ev_in[j].record(s_in)
+        stream.wait_event(ev_in[j])
+        stream.wait_event(ev_out[j])             # the set's previous Y has left for the host
+        y = run_stages(Xd[j], j)
+        ev_done[j].record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_done[j])
+            Yh[j].copy_(y, non_blocking=True)
+            ev_out[j].record(s_out)
 
-    for _ in range(2):
-        e2e_step()
+    for i in range(2):
+        e2e_step(i)
     torch.cuda.synchronize(dev)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
+    s_in.wait_event(e0)
+    for i in range(e2e_steps):
+        e2e_step(i)
+    for j in range(2):
+        stream.wait_event(ev_out[j])
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
@@ -411,6 +434,7 @@ def run_ours(args):
                           "frac": pack_gbs / pk["hbm_gbs"], "bytes_per_launch": pack_bytes,
                           "peak_source": f"{pk['source']} copy bandwidth"},
         "e2e": {"value": job_tops(world, ops, e2e_ms), "unit": "TOPS",
+                "pipelining": "H2D of step i+1 and D2H of step i overlap compute on separate streams",
                 "h2d_bytes_per_step": wl.m * wl.k * 4, "d2h_bytes_per_step": wl.m * n_out * 4,
                 "ms_per_step": e2e_ms},
         "gpu_launches": (2 * len(stages) + (1 if wl.lora_r else 0)) * args.steps,
