@@ -718,11 +718,17 @@ cudaError_t launch_plan(Kernel kern, const Shape sh, const PackArgs &a, cudaStre
 }
 
 
-// Ring form tuning: CTAs per SM, ring bytes per CTA, and CTA size to aim for.
-constexpr int kRingCtasPerSm = 2;
-constexpr uint32_t kRingBytes = 100 * 1024;
-constexpr uint32_t kRingBytesSolo = 200 * 1024;  // one CTA per SM, for long rows
-constexpr int kRingThreadsTarget = 128;
+// Ring form tuning, tried in order: CTAs per SM, ring bytes per CTA and CTA
+// size to aim for. Smaller CTAs with one or two rows per stage balance short
+// rows better over the SMs (K = 3072: 2048 blocks over 608 CTAs instead of
+// 1024 over 304); rows too long for two stages in the first ring take the
+// next.
+struct RingTuning {
+    int ctas_per_sm;
+    uint32_t ring_bytes;
+    int threads_target;
+};
+constexpr RingTuning kRingTunings[] = {{4, 50 * 1024, 64}, {2, 100 * 1024, 128}, {1, 200 * 1024, 128}};
 
 struct RingLaunch {
     RingPlan P;
@@ -731,28 +737,26 @@ struct RingLaunch {
 
 RingLaunch ring_plan(int k)
 {
-    RingLaunch L{};
     const int T = threads_per_row(Shape{2, 16}, k);
     const int step = 32 / gcd_int(T, 32);  // rows per stage must fill whole warps
     const uint64_t row_bytes = 4ull * static_cast<uint64_t>(k);
-    if (step * T > 512) return L;
-    int R = step;
-    while (R * T < kRingThreadsTarget && (R + step) * T <= 512) R += step;
-    uint32_t budget = kRingBytes;
-    L.ctas_per_sm = kRingCtasPerSm;
-    while (R > step && 2ull * R * row_bytes > budget) R -= step;
-    if (2ull * R * row_bytes > budget) {
-        budget = kRingBytesSolo;
-        L.ctas_per_sm = 1;
-        if (2ull * R * row_bytes > budget) return RingLaunch{};
+    if (step * T > 512) return RingLaunch{};
+    for (const RingTuning &tu : kRingTunings) {
+        int R = step;
+        while (R * T < tu.threads_target && (R + step) * T <= 512) R += step;
+        while (R > step && 2ull * R * row_bytes > tu.ring_bytes) R -= step;
+        if (2ull * R * row_bytes > tu.ring_bytes) continue;
+        RingLaunch L{};
+        L.ctas_per_sm = tu.ctas_per_sm;
+        L.P.threads_per_row = T;
+        L.P.rows_per_stage = R;
+        L.P.row_bytes = static_cast<uint32_t>(row_bytes);
+        L.P.stage_bytes = static_cast<uint32_t>(R * row_bytes);
+        const int ns = static_cast<int>(tu.ring_bytes / L.P.stage_bytes);
+        L.P.stages = ns > kMaxStages ? kMaxStages : ns;
+        return L;
     }
-    L.P.threads_per_row = T;
-    L.P.rows_per_stage = R;
-    L.P.row_bytes = static_cast<uint32_t>(row_bytes);
-    L.P.stage_bytes = static_cast<uint32_t>(R * row_bytes);
-    const int ns = static_cast<int>(budget / L.P.stage_bytes);
-    L.P.stages = ns > kMaxStages ? kMaxStages : ns;
-    return L;
+    return RingLaunch{};
 }
 
 template <typename Kernel>
