@@ -48,7 +48,8 @@ typedef enum {
     CONVROT_ERR_K_RANGE = 4,     /* k < 1 or k > CONVROT_MAX_K */
     CONVROT_ERR_CUDA = 5,        /* a kernel launch failed */
     CONVROT_ERR_TIMEOUT = 6,     /* written to *dev_status by a kernel whose bounded wait ran out */
-    CONVROT_ERR_UNSUPPORTED = 7  /* valid request this build has no kernel for */
+    CONVROT_ERR_UNSUPPORTED = 7, /* valid request this build has no kernel for */
+    CONVROT_ERR_SCRATCH = 8      /* larger than the static scratch of convrot_linear_lora_noalloc */
 } convrot_status;
 
 /* Largest k: 127 * 127 * k must fit in a signed 32-bit accumulator ("Runtime
@@ -231,6 +232,29 @@ convrot_status convrot_lora_down(const float *X, int64_t m, int64_t k, int64_t l
 convrot_status convrot_linear_lora(const convrot_packed *x, const convrot_packed *w, const float *bias, int32_t act,
                                    const void *T_ext, int64_t ldt, const void *B_ext, int64_t lde, int32_t r,
                                    float *Y, int64_t ldy, int32_t *dev_status, cudaStream_t stream);
+
+/*
+ * No counterpart on the page (an entry point of this library only): the LoRA
+ * linear in one call that allocates nothing, not even T_ext. It runs
+ * convrot_lora_down into a file-scope device array of the library
+ * (CONVROT_NOALLOC_SCRATCH_BYTES, 256-byte aligned; its address comes from
+ * cudaGetSymbolAddress on the current device), then convrot_linear_lora
+ * reading it. Results equal those of the two calls with a caller's T_ext.
+ *   X, ldx, A_ext, lda, k = x->k   as for convrot_lora_down.
+ *   B_ext, lde, r, bias, act, Y, ldy, dev_status   as for convrot_linear_lora.
+ * A request whose T_ext (x->rows * convrot_lora_cols(r) bf16) exceeds the
+ * array returns CONVROT_ERR_SCRATCH and launches nothing; a failed address
+ * lookup returns CONVROT_ERR_CUDA. Nothing in the array must start at zero
+ * (the down kernel writes every column the GEMM reads, padding included).
+ * The array is one per device and process: calls that overlap in time (on
+ * different streams, or from different host threads) race on it; serialize
+ * them, e.g. on one stream.
+ */
+#define CONVROT_NOALLOC_SCRATCH_BYTES (32ll << 20)
+convrot_status convrot_linear_lora_noalloc(const convrot_packed *x, const convrot_packed *w, const float *bias,
+                                           int32_t act, const float *X, int64_t ldx, const float *A_ext, int64_t lda,
+                                           const void *B_ext, int64_t lde, int32_t r, float *Y, int64_t ldy,
+                                           int32_t *dev_status, cudaStream_t stream);
 
 /*
  * The integer GEMM alone: A[r, o] = sum_i Q_x[r, i] * Q_w[o, i] as int32, for

@@ -17,7 +17,8 @@ import torch
 
 from . import build as _build
 
-OK, ERR_INVALID_ARG, ERR_GROUP_SIZE, ERR_ALIGNMENT, ERR_K_RANGE, ERR_CUDA, ERR_TIMEOUT, ERR_UNSUPPORTED = range(8)
+OK, ERR_INVALID_ARG, ERR_GROUP_SIZE, ERR_ALIGNMENT, ERR_K_RANGE, ERR_CUDA, ERR_TIMEOUT, ERR_UNSUPPORTED, ERR_SCRATCH = range(9)
+NOALLOC_SCRATCH_BYTES = 32 << 20
 CODES_I8, CODES_BF16 = 0, 1
 MAX_K = 133144
 MAX_GROUP = 4096
@@ -33,6 +34,7 @@ EXPORTED = [
     "convrot_lora_prepare_down",
     "convrot_lora_down",
     "convrot_linear_lora",
+    "convrot_linear_lora_noalloc",
     "convrot_gemm_i32",
     "convrot_status_string",
 ]
@@ -96,6 +98,8 @@ def load() -> ctypes.CDLL:
         lib.convrot_lora_down.restype = ctypes.c_int
         lib.convrot_linear_lora.argtypes = [P, P, vp, i32, vp, i64, vp, i64, i32, vp, i64, vp, vp]
         lib.convrot_linear_lora.restype = ctypes.c_int
+        lib.convrot_linear_lora_noalloc.argtypes = [P, P, vp, i32, vp, i64, vp, i64, vp, i64, i32, vp, i64, vp, vp]
+        lib.convrot_linear_lora_noalloc.restype = ctypes.c_int
         lib.convrot_gemm_i32.argtypes = [P, P, vp, i64, vp, vp]
         lib.convrot_gemm_i32.restype = ctypes.c_int
         lib.convrot_status_string.argtypes = [ctypes.c_int]
@@ -297,6 +301,24 @@ def convrot_linear_lora(x: Packed, w: Packed, bias: torch.Tensor | None, act: in
                                       t_ext.stride(0), _ptr(b_ext), b_ext.stride(0), int(r), _ptr(out),
                                       out.stride(0) if out.dim() == 2 else 0, _ptr(dev_status), _stream(stream)),
            "convrot_linear_lora")
+    return out
+
+
+def convrot_linear_lora_noalloc(x: Packed, w: Packed, bias: torch.Tensor | None, act: int, X: torch.Tensor,
+                                A_ext: torch.Tensor, b_ext: torch.Tensor, r: int, out: torch.Tensor | None = None,
+                                dev_status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """The LoRA linear in one call, T_ext in the library's static device scratch (nothing
+    allocated; calls that overlap in time race on that scratch)."""
+    if out is None:
+        out = _padded_out(x.rows, w.rows, torch.float32, x.q.device)
+    if bias is not None and (bias.dtype != torch.float32 or not bias.is_cuda):
+        raise TypeError("bias must be a float32 CUDA tensor")
+    xs, ws = x.struct(), w.struct()
+    _check(load().convrot_linear_lora_noalloc(ctypes.byref(xs), ctypes.byref(ws), _ptr(bias), int(act), _ptr(X),
+                                              X.stride(0), _ptr(A_ext), A_ext.stride(0), _ptr(b_ext),
+                                              b_ext.stride(0), int(r), _ptr(out),
+                                              out.stride(0) if out.dim() == 2 else 0, _ptr(dev_status),
+                                              _stream(stream)), "convrot_linear_lora_noalloc")
     return out
 
 

@@ -8,6 +8,9 @@
 
 namespace {
 
+// Scratch of convrot_linear_lora_noalloc: T_ext, one array per device.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[CONVROT_NOALLOC_SCRATCH_BYTES];
+
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 // Returns n for G = 4^n (n >= 1, G <= CONVROT_MAX_GROUP), else -1.
@@ -251,6 +254,25 @@ convrot_status convrot_linear_lora(const convrot_packed *x, const convrot_packed
     return run_gemm(x, w, bias, Y, nullptr, ldy, act, dev_status, stream, lora);
 }
 
+convrot_status convrot_linear_lora_noalloc(const convrot_packed *x, const convrot_packed *w, const float *bias,
+                                           int32_t act, const float *X, int64_t ldx, const float *A_ext, int64_t lda,
+                                           const void *B_ext, int64_t lde, int32_t r, float *Y, int64_t ldy,
+                                           int32_t *dev_status, cudaStream_t stream)
+{
+    if (!x || !w) return CONVROT_ERR_INVALID_ARG;
+    if (!lora_rank_ok(r)) return CONVROT_ERR_INVALID_ARG;
+    const int64_t cols = convrot_lora_cols(r);
+    if (x->rows < 0) return CONVROT_ERR_INVALID_ARG;
+    if (x->rows > CONVROT_NOALLOC_SCRATCH_BYTES / (cols * 2)) return CONVROT_ERR_SCRATCH;
+    if (x->rows == 0 || w->rows == 0) return convrot_linear_lora(x, w, bias, act, nullptr, cols, B_ext, lde, r, Y, ldy,
+                                                                 dev_status, stream);
+    void *scratch = nullptr;
+    if (cudaGetSymbolAddress(&scratch, g_noalloc_scratch) != cudaSuccess || !scratch) return CONVROT_ERR_CUDA;
+    convrot_status st = convrot_lora_down(X, x->rows, x->k, ldx, A_ext, r, lda, scratch, cols, dev_status, stream);
+    if (st != CONVROT_OK) return st;
+    return convrot_linear_lora(x, w, bias, act, scratch, cols, B_ext, lde, r, Y, ldy, dev_status, stream);
+}
+
 convrot_status convrot_gemm_i32(const convrot_packed *x, const convrot_packed *w, int32_t *A,
                                 int64_t lda, int32_t *dev_status, cudaStream_t stream)
 {
@@ -269,6 +291,7 @@ const char *convrot_status_string(convrot_status s)
     case CONVROT_ERR_CUDA: return "CUDA launch failed";
     case CONVROT_ERR_TIMEOUT: return "a kernel gave up a bounded wait";
     case CONVROT_ERR_UNSUPPORTED: return "no kernel for this request in this build";
+    case CONVROT_ERR_SCRATCH: return "request larger than the static scratch of the no-allocation entry point";
     default: return "unknown status";
     }
 }

@@ -1,0 +1,62 @@
+"""convrot_linear_lora_noalloc: the LoRA linear with T_ext in the library's
+static device scratch. Two calls in a row (different shapes and ranks, so the
+second reuses scratch the first wrote) must equal the two-call path with a
+caller-provided T_ext, bit for bit: the same kernels run on the same inputs."""
+
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from int8_hadamard_rotated_convrot_gb300 import build as cbuild
+from int8_hadamard_rotated_convrot_gb300 import convrot as cr
+
+FAKE = 0x10000
+
+
+def test_noalloc_rejects_requests_beyond_the_scratch():
+    cbuild.build()
+    lib = cr.load()
+    r = 64
+    cols = lib.convrot_lora_cols(r)
+    rows = cr.NOALLOC_SCRATCH_BYTES // (cols * 2) + 1
+    ld = cr.convrot_ldq(256)
+    x = cr._Packed(FAKE, FAKE, rows, 256, ld, 256, cr.CODES_BF16)
+    w = cr._Packed(FAKE, FAKE, 8, 256, ld, 256, cr.CODES_BF16)
+    st = lib.convrot_linear_lora_noalloc(ctypes.byref(x), ctypes.byref(w), None, 0, FAKE, 256, FAKE, 256, FAKE, cols,
+                                         r, FAKE, 8, None, None)
+    assert st == cr.ERR_SCRATCH
+    assert "static scratch" in cr.status_string(cr.ERR_SCRATCH)
+    assert lib.convrot_linear_lora_noalloc(ctypes.byref(x), ctypes.byref(w), None, 0, FAKE, 256, FAKE, 256, FAKE,
+                                           cols, 20, FAKE, 8, None, None) == cr.ERR_INVALID_ARG
+
+
+def _case(rng, m, n, k, r):
+    X = rng.standard_normal((m, k)).astype(np.float32)
+    W = (0.02 * rng.standard_normal((n, k))).astype(np.float32)
+    b = rng.standard_normal(n).astype(np.float32)
+    A = (0.05 * rng.standard_normal((r, k))).astype(np.float32)
+    B = (0.05 * rng.standard_normal((n, r))).astype(np.float32)
+    dev = lambda a: torch.from_numpy(a).cuda()
+    Xd = dev(X)
+    px = cr.convrot_pack_activations(Xd, 64, cr.CODES_BF16)
+    pw = cr.convrot_quantize_weights(dev(W), 64, cr.CODES_BF16)
+    A_ext = cr.convrot_lora_prepare_down(dev(A))
+    B_ext = cr.convrot_lora_prepare(dev(B), 2.0)
+    return Xd, px, pw, dev(b), A_ext, B_ext
+
+
+@pytest.mark.gpu
+def test_noalloc_lora_linear_twice_equals_two_call_path():
+    rng = np.random.default_rng(2024)
+    cases = [(_case(rng, 300, 512, 1024, 64), 64, cr.ACT_NONE), (_case(rng, 129, 256, 512, 32), 32, cr.ACT_GELU_ERF)]
+    outs = []
+    for (Xd, px, pw, b, A_ext, B_ext), r, act in cases:  # two calls in a row
+        outs.append(cr.convrot_linear_lora_noalloc(px, pw, b, act, Xd, A_ext, B_ext, r))
+    for ((Xd, px, pw, b, A_ext, B_ext), r, act), y in zip(cases, outs):
+        T_ext = cr.convrot_lora_down(Xd, A_ext)
+        y_ref = cr.convrot_linear_lora(px, pw, b, act, T_ext, B_ext, r)
+        torch.cuda.synchronize()
+        assert torch.equal(y, y_ref)
+        assert torch.isfinite(y).all() and y.abs().max() > 0
