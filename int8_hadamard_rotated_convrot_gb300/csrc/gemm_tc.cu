@@ -151,8 +151,6 @@ __device__ __forceinline__ void store_tile_rows(const TcParams &p, const CUtenso
         if (cc * 32 >= ncols) break;
         const int64_t x = col0 + cc * 32;
         if (x >= p.n) break;
-        uint32_t lr[kLora ? 32 : 1];
-        if constexpr (kLora) tmem_ld32(lora_taddr + cc * 32, lr);
         if ((kAct != 0 || kLora) && x + 32 > p.n) {
             // ragged last box with an activation or a LoRA term: stage, activate, then masked stores
             const uint32_t buf = out_smem + (store_iter & 1u) * OUT_BUF_BYTES;
@@ -160,14 +158,15 @@ __device__ __forceinline__ void store_tile_rows(const TcParams &p, const CUtenso
             __syncwarp();
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
-                uint32_t w[4];
+                uint32_t w[4], lr[4];
+                if constexpr (kLora) tmem_ld4(lora_taddr + cc * 32 + c * 4, lr);
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int64_t col = x + c * 4 + e;
                     const float swv = col < p.n ? __ldg(p.sw + col) : 0.0f;
                     const float bv = (p.bias && col < p.n) ? __ldg(p.bias + col) : 0.0f;
                     float y = fmaf(static_cast<float>(acc[cc * 32 + c * 4 + e]) * sxr, swv, bv);
-                    if constexpr (kLora) y += __uint_as_float(lr[c * 4 + e]);
+                    if constexpr (kLora) y += __uint_as_float(lr[e]);
                     w[e] = __float_as_uint(y);
                 }
                 const uint32_t addr = buf + lane * (OUT_BOX * 4) + ((c ^ (lane & 7)) << 4);
@@ -208,7 +207,8 @@ __device__ __forceinline__ void store_tile_rows(const TcParams &p, const CUtenso
         __syncwarp();
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
-            uint32_t w[4];
+            uint32_t w[4], lr[4];
+            if constexpr (kLora) tmem_ld4(lora_taddr + cc * 32 + c * 4, lr);
             float4 sw4 = make_float4(0.f, 0.f, 0.f, 0.f), b4 = make_float4(0.f, 0.f, 0.f, 0.f);
             if constexpr (!kRawInt32) {
                 const int64_t col = x + c * 4;
@@ -230,7 +230,7 @@ __device__ __forceinline__ void store_tile_rows(const TcParams &p, const CUtenso
                     w[e] = static_cast<uint32_t>(acc[j]);
                 } else {
                     float y = fmaf(static_cast<float>(acc[j]) * sxr, swv[e], bv[e]);
-                    if constexpr (kLora) y += __uint_as_float(lr[c * 4 + e]);
+                    if constexpr (kLora) y += __uint_as_float(lr[e]);
                     w[e] = __float_as_uint(y);
                 }
             }
