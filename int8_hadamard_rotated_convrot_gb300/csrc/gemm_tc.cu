@@ -231,6 +231,7 @@ __device__ __forceinline__ void store_tile_rows(const TcParams &p, const CUtenso
                 } else {
                     float y = fmaf(static_cast<float>(acc[j]) * sxr, swv[e], bv[e]);
                     if constexpr (kLora) y += __uint_as_float(lr[e]);
+                    if constexpr (kAct != 0) y = apply_act_t<kAct>(y);  // short and call-free: applied in place
                     w[e] = __float_as_uint(y);
                 }
             }
@@ -239,7 +240,6 @@ __device__ __forceinline__ void store_tile_rows(const TcParams &p, const CUtenso
                          "r"(w[3])
                          : "memory");
         }
-        if constexpr (kAct != 0) act_box<kAct>(buf, lane);
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
         if (lane == 0) {

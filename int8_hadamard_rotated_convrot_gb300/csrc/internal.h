@@ -57,10 +57,33 @@ cudaError_t launch_lora_down(const float *X, int64_t m, int32_t k, int64_t ldx, 
                              int64_t lda, void *t, int64_t ldt, int32_t *dev_status, cudaStream_t stream);
 
 // GELU, erf or tanh form (convrot_activation), on the epilogue's fp32 value.
+// The tanh form is evaluated through its exact identity
+// 0.5 v (1 + tanh(u)) = v / (1 + e^(-2u)), u = sqrt(2/pi) (v + 0.044715 v^3):
+// one fast exponential and one fast division. Its relative error, a few 2^-22
+// over the range where the result is not negligible, stays inside the
+// epilogue's tolerance. (As v -> -inf, e^(-2u) overflows and __fdividef
+// returns 0; the result is then -0 or 0, as GELU's value there rounds to.)
+// The erf form uses Abramowitz & Stegun, Handbook of Mathematical Functions,
+// formula 7.1.26 (|error in erf| <= 1.5e-7): erf(x) = 1 - t (a1 + t (a2 + t (a3
+// + t (a4 + t a5)))) e^(-x^2), t = 1 / (1 + p x), for x >= 0, odd in x. It is
+// call-free, so the epilogue can apply it in place.
+__device__ __forceinline__ float erf_as7126(float x)
+{
+    const float ax = fabsf(x);
+    const float t = __fdividef(1.0f, fmaf(0.3275911f, ax, 1.0f));
+    const float poly =
+        t * fmaf(t, fmaf(t, fmaf(t, fmaf(t, 1.061405429f, -1.453152027f), 1.421413741f), -0.284496736f),
+                 0.254829592f);
+    return copysignf(fmaf(-poly, __expf(-ax * ax), 1.0f), x);
+}
+
 __device__ __forceinline__ float apply_act(float v, int act)
 {
-    if (act == 1) return 0.5f * v * (1.0f + erff(v * 0.70710678118654752f));
-    if (act == 2) return 0.5f * v * (1.0f + tanhf(0.79788456080286536f * fmaf(0.044715f * v, v * v, v)));
+    if (act == 1) return 0.5f * v * (1.0f + erf_as7126(v * 0.70710678118654752f));
+    if (act == 2) {
+        const float u2 = -1.5957691216057308f * fmaf(0.044715f * v, v * v, v);  // -2u
+        return __fdividef(v, 1.0f + __expf(u2));
+    }
     return v;
 }
 
