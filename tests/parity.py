@@ -67,7 +67,8 @@ def check_y_same_codes(y_gpu: np.ndarray, y64_ref: np.ndarray, A: np.ndarray, sx
 def check_y_act_same_codes(y_gpu: np.ndarray, y64_ref: np.ndarray, A: np.ndarray, sx, sw, bias):
     """Y = act(A s_x s_w + b), given identical codes: the pre-activation rule
     (1e-6 of |A s_x s_w| + |b|) times GELU's largest slope (1.13), rounded up
-    to 1.5e-6, plus 3e-7 |Y| for erff/tanhf and the fp32 products after them."""
+    to 1.5e-6 (this also covers the erf approximation's 1.5e-7 |v| / 2), plus
+    3e-7 |Y| for the fast exponential and division and the fp32 products."""
     base = np.abs(A.astype(np.float64) * np.asarray(sx, np.float64)[:, None]
                   * np.asarray(sw, np.float64)[None, :])
     if bias is not None:
