@@ -337,11 +337,25 @@ __device__ __forceinline__ float lane_c0(int l) { return (l == 0 || l == 3) ? 1.
 __device__ __forceinline__ float lane_c1(int l) { return (l == 0 || l == 3) ? -1.0f : 1.0f; }
 __device__ __forceinline__ int lane_out(int l) { return ((l & 1) << 1) | (l >> 1); }
 
-__device__ __forceinline__ void h4_lanes(float &v, float c0, float c1)
+// One base-4 digit held by lane bits (m0, m1 the xor masks of its two bits).
+__device__ __forceinline__ void h4_lanes(float &v, float c0, float c1, int m0, int m1)
 {
-    v = fmaf(c0, v, __shfl_xor_sync(kFull, v, 1));
-    v = fmaf(c1, v, __shfl_xor_sync(kFull, v, 2));
+    v = fmaf(c0, v, __shfl_xor_sync(kFull, v, m0));
+    v = fmaf(c1, v, __shfl_xor_sync(kFull, v, m1));
 }
+
+// Tile layout of the G <= 1024 kernels: 2^LB lanes x 16 float4 slots, quad
+// tile * 16 * 2^LB + 2^LB j + l in slot j. G <= 256 takes LB = 2 (one lane
+// digit); G = 1024 takes LB = 4, two lane digits (lane bits 0-1 and 2-3) and
+// the slot digits above them. A lane digit's butterfly partners share every
+// other digit, so the signs the two lane digits carry simply multiply, and
+// each lane digit permutes its own part of the output quad.
+template <int N>
+struct Tile {
+    static constexpr int LB = N == 5 ? 4 : 2;
+    static constexpr int LANES = 1 << LB;
+    static constexpr int QUADS = 16 << LB;
+};
 
 // Round half away from zero of the exact product v * inv: with h = +-1/2
 // carrying the product's sign, the fma rounded toward zero never crosses the
@@ -358,19 +372,30 @@ __device__ __forceinline__ float code_of(float v, float inv, uint32_t half_bits)
 template <int N>
 __device__ __forceinline__ void rotate_g256(float4 (&v)[16], int l)
 {
+    constexpr int LB = Tile<N>::LB;
 #pragma unroll
     for (int j = 0; j < 16; ++j) h4_regs(v[j].x, v[j].y, v[j].z, v[j].w);  // digit 0
-    if constexpr (N >= 2) {                                                  // digit 1
-        const float c0 = lane_c0(l), c1 = lane_c1(l);
+    if constexpr (N >= 2) {                                                  // digit 1: lane bits 0-1
+        const float c0 = lane_c0(l & 3), c1 = lane_c1(l & 3);
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
-            h4_lanes(v[j].x, c0, c1);
-            h4_lanes(v[j].y, c0, c1);
-            h4_lanes(v[j].z, c0, c1);
-            h4_lanes(v[j].w, c0, c1);
+            h4_lanes(v[j].x, c0, c1, 1, 2);
+            h4_lanes(v[j].y, c0, c1, 1, 2);
+            h4_lanes(v[j].z, c0, c1, 1, 2);
+            h4_lanes(v[j].w, c0, c1, 1, 2);
         }
     }
-    if constexpr (N >= 3) {  // digit 2: slots 4 b + (0..3)
+    if constexpr (LB == 4) {  // digit 2: lane bits 2-3
+        const float c0 = lane_c0((l >> 2) & 3), c1 = lane_c1((l >> 2) & 3);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            h4_lanes(v[j].x, c0, c1, 4, 8);
+            h4_lanes(v[j].y, c0, c1, 4, 8);
+            h4_lanes(v[j].z, c0, c1, 4, 8);
+            h4_lanes(v[j].w, c0, c1, 4, 8);
+        }
+    }
+    if constexpr (N >= LB / 2 + 2) {  // the first slot digit: slots 4 b + (0..3)
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
             float4 &p0 = v[4 * b], &p1 = v[4 * b + 1], &p2 = v[4 * b + 2], &p3 = v[4 * b + 3];
@@ -380,7 +405,7 @@ __device__ __forceinline__ void rotate_g256(float4 (&v)[16], int l)
             h4_regs(p0.w, p1.w, p2.w, p3.w);
         }
     }
-    if constexpr (N >= 4) {  // digit 3: slots b + 4 (0..3)
+    if constexpr (N >= LB / 2 + 3) {  // the second slot digit: slots b + 4 (0..3)
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
             float4 &p0 = v[b], &p1 = v[b + 4], &p2 = v[b + 8], &p3 = v[b + 12];
@@ -401,14 +426,20 @@ __device__ __forceinline__ float absmax_g256(const float4 (&v)[16])
     return m;
 }
 
-// Codes of slots j < nv. q0 is the thread's slot-0 quad (tile * 64 + l); inv the
-// multiplier from scale_of.
+// Codes of slots j < nv. q0 is the thread's slot-0 quad (tile * QUADS + l); inv
+// the multiplier from scale_of.
 template <int N, bool kBf16>
 __device__ __forceinline__ void store_g256(const float4 (&v)[16], int nv, int l, int q0, char *qrow, float inv)
 {
-    if constexpr (N >= 2) inv *= lane_c1(l);  // the kept value's sign times D1 at the output
+    constexpr int LB = Tile<N>::LB, LANES = Tile<N>::LANES;
+    // the kept value's sign times D1 at the output, for each lane digit
+    if constexpr (N >= 2) inv *= lane_c1(l & 3);
+    if constexpr (LB == 4) inv *= lane_c1((l >> 2) & 3);
     const uint32_t half_bits = 0x3f000000u | (__float_as_uint(inv) & kSign);
-    const int qo = q0 - l + (N >= 2 ? lane_out(l) : l);
+    int lo = l;  // P on each lane digit
+    if constexpr (N >= 2) lo = lane_out(l & 3) | (l & ~3);
+    if constexpr (LB == 4) lo = lane_out(l & 3) | (lane_out((l >> 2) & 3) << 2);
+    const int qo = q0 - l + lo;
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
         if (j >= nv) break;
@@ -418,22 +449,23 @@ __device__ __forceinline__ void store_g256(const float4 (&v)[16], int nv, int l,
             // |r| <= 127: the bf16 of r is the top half of its fp32 bits (a zero code may be -0)
             const uint32_t lo = __byte_perm(__float_as_uint(r0), __float_as_uint(r1), 0x7632);
             const uint32_t hi = __byte_perm(__float_as_uint(r2), __float_as_uint(r3), 0x7632);
-            reinterpret_cast<uint2 *>(qrow)[qo + 4 * j] = make_uint2(lo, hi);
+            reinterpret_cast<uint2 *>(qrow)[qo + LANES * j] = make_uint2(lo, hi);
         } else {
             // r + 1.5 * 2^23 holds r in its low mantissa bits: the low byte is r as int8
             constexpr float kMagic = 12582912.0f;
             const uint32_t w0 = __float_as_uint(r0 + kMagic), w1 = __float_as_uint(r1 + kMagic);
             const uint32_t w2 = __float_as_uint(r2 + kMagic), w3 = __float_as_uint(r3 + kMagic);
-            reinterpret_cast<uint32_t *>(qrow)[qo + 4 * j] =
+            reinterpret_cast<uint32_t *>(qrow)[qo + LANES * j] =
                 __byte_perm(__byte_perm(w0, w1, 0x0040), __byte_perm(w2, w3, 0x0040), 0x5410);
         }
     }
 }
 
-// Slots holding data: quad q0 + 4 j < kq. Whole groups are in or out.
+// Slots holding data: quad q0 + 2^LB j < kq. Whole groups are in or out.
+template <int LB>
 __device__ __forceinline__ int valid_slots(int kq, int q0)
 {
-    const int nv = (kq - q0 + 3) >> 2;
+    const int nv = (kq - q0 + (1 << LB) - 1) >> LB;
     return nv < 0 ? 0 : (nv > 16 ? 16 : nv);
 }
 
@@ -471,14 +503,16 @@ __global__ void __launch_bounds__(512) pack_g256_kernel(PackArgs a, DirectPlan L
     const bool row_ok = row < a.rows;
     const int t_row = cr * tpr + t_cta;
     const int kq = a.k >> 2, kpq = a.kpad >> 2;
-    const int l = t_row & 3;
-    const int q0 = (t_row >> 2) * 64 + l;
-    const int nv = row_ok ? valid_slots(kq, q0) : 0;
+    constexpr int LB = Tile<N>::LB;
+    const int l = t_row & (Tile<N>::LANES - 1);
+    const int q0 = (t_row >> LB) * Tile<N>::QUADS + l;
+    const int nv = row_ok ? valid_slots<LB>(kq, q0) : 0;
 
     const float4 *src = reinterpret_cast<const float4 *>(a.x + (row_ok ? row : 0) * a.ldx) + q0;
     float4 v[16];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) v[j] = j < nv ? __ldcs(src + 4 * j) : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < 16; ++j)
+        v[j] = j < nv ? __ldcs(src + Tile<N>::LANES * j) : make_float4(0.f, 0.f, 0.f, 0.f);
     rotate_g256<N>(v, l);
 
     __shared__ float part[128];
@@ -563,9 +597,10 @@ __global__ void __launch_bounds__(512) pack_ring_kernel(PackArgs a, RingPlan P)
     const int r_local = threadIdx.x / tpr;
     const int t_row = threadIdx.x - r_local * tpr;
     const int kq = a.k >> 2, kpq = a.kpad >> 2;
-    const int l = t_row & 3;
-    const int q0 = (t_row >> 2) * 64 + l;
-    const int nv = valid_slots(kq, q0);
+    constexpr int LB = Tile<N>::LB;
+    const int l = t_row & (Tile<N>::LANES - 1);
+    const int q0 = (t_row >> LB) * Tile<N>::QUADS + l;
+    const int nv = valid_slots<LB>(kq, q0);
     const int64_t nblocks = (a.rows + R - 1) / R;
     const uint32_t ring_base = static_cast<uint32_t>(__cvta_generic_to_shared(ring));
     const uint32_t bar_base = static_cast<uint32_t>(__cvta_generic_to_shared(full_bar));
@@ -610,7 +645,8 @@ __global__ void __launch_bounds__(512) pack_ring_kernel(PackArgs a, RingPlan P)
         const float4 *src = reinterpret_cast<const float4 *>(ring + stage * P.stage_bytes + r_local * P.row_bytes) + q0;
         float4 v[16];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) v[j] = (row_ok && j < nv) ? src[4 * j] : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j = 0; j < 16; ++j)
+            v[j] = (row_ok && j < nv) ? src[Tile<N>::LANES * j] : make_float4(0.f, 0.f, 0.f, 0.f);
         rotate_g256<N>(v, l);
         float *pp = part[it & 1];
         row_max_write(absmax_g256(v), tpr, pp);
@@ -735,9 +771,9 @@ struct RingLaunch {
     int ctas_per_sm;  // 0: rows too long for a ring
 };
 
-RingLaunch ring_plan(int k)
+RingLaunch ring_plan(int k, int lane_bits)
 {
-    const int T = threads_per_row(Shape{2, 16}, k);
+    const int T = threads_per_row(Shape{lane_bits, 16}, k);
     const int step = 32 / gcd_int(T, 32);  // rows per stage must fill whole warps
     const uint64_t row_bytes = 4ull * static_cast<uint64_t>(k);
     if (step * T > 512) return RingLaunch{};
@@ -780,9 +816,9 @@ cudaError_t launch_ring(Kernel kern, const RingLaunch &L, const PackArgs &a, cud
 template <int N, bool kBf16>
 cudaError_t launch_g256(const PackArgs &a, cudaStream_t stream)
 {
-    const RingLaunch L = ring_plan(a.k);
+    const RingLaunch L = ring_plan(a.k, Tile<N>::LB);
     if (L.ctas_per_sm > 0) return launch_ring(pack_ring_kernel<N, kBf16>, L, a, stream);
-    return launch_plan(pack_g256_kernel<N, kBf16>, Shape{2, 16}, a, stream);
+    return launch_plan(pack_g256_kernel<N, kBf16>, Shape{Tile<N>::LB, 16}, a, stream);
 }
 
 template <bool kBf16>
@@ -793,7 +829,7 @@ cudaError_t dispatch(const PackArgs &a, cudaStream_t stream)
     case 2: return launch_g256<2, kBf16>(a, stream);
     case 3: return launch_g256<3, kBf16>(a, stream);
     case 4: return launch_g256<4, kBf16>(a, stream);
-    case 5: return launch_plan(pack_kernel<5, 8, kBf16>, Shape{5, 8}, a, stream);    // G = 1024
+    case 5: return launch_g256<5, kBf16>(a, stream);                                 // G = 1024
     case 6: return launch_plan(pack_kernel<5, 32, kBf16>, Shape{5, 32}, a, stream);  // G = 4096
     default: return cudaErrorInvalidValue;
     }

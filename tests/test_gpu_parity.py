@@ -99,12 +99,15 @@ def test_pack_matches_oracle(G, k, codes):
     assert float(p.scale[0]) == 0.0 and torch.all(p.q[0, :cr.convrot_ldq(k)] == 0)
 
 
-@pytest.mark.parametrize("G,k,m", [(256, 768, 3000), (4, 768, 3000), (64, 16384, 700), (256, 28672, 40)],
-                         ids=["ring-wraps", "ring-wraps-G4", "ring-one-cta-per-sm", "direct"])
+@pytest.mark.parametrize("G,k,m", [(256, 768, 3000), (4, 768, 3000), (64, 16384, 700), (256, 28672, 40),
+                                   (1024, 3072, 3000), (1024, 16384, 500), (1024, 28672, 40)],
+                         ids=["ring-wraps", "ring-wraps-G4", "ring-one-cta-per-sm", "direct",
+                              "G1024-ring", "G1024-ring-one-cta", "G1024-direct"])
 @pytest.mark.parametrize("codes", CODES, ids=CODE_IDS)
 def test_pack_launch_forms(G, k, m, codes):
-    """Each launch form of the G <= 256 pack: a shared-memory ring that wraps many
-    times, a ring of one CTA per SM (long rows), and the direct form."""
+    """Each launch form of the G <= 1024 pack: a shared-memory ring that wraps many
+    times, a ring of one CTA per SM (long rows), and the direct form; G = 1024
+    uses 16-lane tiles with two lane digits."""
     rng = np.random.default_rng(G + k + m)
     X = special_rows(rng, m, k)
     p = gpu_pack(X, G, codes)
