@@ -265,6 +265,22 @@ convrot_status convrot_linear_lora_noalloc(const convrot_packed *x, const convro
 convrot_status convrot_gemm_i32(const convrot_packed *x, const convrot_packed *w, int32_t *A,
                                 int64_t lda, int32_t *dev_status, cudaStream_t stream);
 
+/*
+ * No counterpart on the page (an entry point of this library only): checks
+ * failure detection without a fault. One CTA waits on an mbarrier through
+ * the same bounded wait that the GEMM, LoRA and ring-pack kernels use on
+ * their copies and MMAs (those use the limit CONVROT_WAIT_LIMIT_NS).
+ *   dev_status  device int32, non-NULL. With arrive == 0 nothing arrives:
+ *               the wait gives up after limit_ns and the kernel writes
+ *               CONVROT_ERR_TIMEOUT there, as those kernels do on a stall.
+ *               With arrive != 0 the wait ends at once and it is untouched.
+ *   limit_ns    in (0, CONVROT_WAIT_LIMIT_NS]; anything else is
+ *               CONVROT_ERR_INVALID_ARG and launches nothing.
+ * The kernel returns normally either way; the context stays usable.
+ */
+#define CONVROT_WAIT_LIMIT_NS 4000000000ull
+convrot_status convrot_wait_check(int32_t *dev_status, uint64_t limit_ns, int32_t arrive, cudaStream_t stream);
+
 /* Static, NUL-terminated description of a status. Never NULL. */
 const char *convrot_status_string(convrot_status status);
 

@@ -19,6 +19,7 @@ from . import build as _build
 
 OK, ERR_INVALID_ARG, ERR_GROUP_SIZE, ERR_ALIGNMENT, ERR_K_RANGE, ERR_CUDA, ERR_TIMEOUT, ERR_UNSUPPORTED, ERR_SCRATCH = range(9)
 NOALLOC_SCRATCH_BYTES = 32 << 20
+WAIT_LIMIT_NS = 4_000_000_000
 CODES_I8, CODES_BF16 = 0, 1
 MAX_K = 133144
 MAX_GROUP = 4096
@@ -36,6 +37,7 @@ EXPORTED = [
     "convrot_linear_lora",
     "convrot_linear_lora_noalloc",
     "convrot_gemm_i32",
+    "convrot_wait_check",
     "convrot_status_string",
 ]
 
@@ -102,6 +104,8 @@ def load() -> ctypes.CDLL:
         lib.convrot_linear_lora_noalloc.restype = ctypes.c_int
         lib.convrot_gemm_i32.argtypes = [P, P, vp, i64, vp, vp]
         lib.convrot_gemm_i32.restype = ctypes.c_int
+        lib.convrot_wait_check.argtypes = [vp, ctypes.c_uint64, i32, vp]
+        lib.convrot_wait_check.restype = ctypes.c_int
         lib.convrot_status_string.argtypes = [ctypes.c_int]
         lib.convrot_status_string.restype = ctypes.c_char_p
         _lib = lib
@@ -332,6 +336,14 @@ def convrot_gemm_i32(x: Packed, w: Packed, out: torch.Tensor | None = None,
                                    out.stride(0) if out.dim() == 2 else 0, _ptr(dev_status),
                                    _stream(stream)), "convrot_gemm_i32")
     return out
+
+
+def convrot_wait_check(dev_status: torch.Tensor, limit_ns: int, arrive: bool, stream=None) -> None:
+    """Launch the bounded-wait check: with arrive False the kernel's wait runs
+    out after limit_ns and it writes ERR_TIMEOUT into dev_status (int32, one
+    element); with arrive True dev_status is left as it is."""
+    _check(load().convrot_wait_check(_ptr(dev_status), int(limit_ns), int(bool(arrive)), _stream(stream)),
+           "convrot_wait_check")
 
 
 def quantize_weights_grouped(Ws, G: int, codes: int = CODES_I8, stream=None) -> Packed:

@@ -280,6 +280,13 @@ convrot_status convrot_gemm_i32(const convrot_packed *x, const convrot_packed *w
     return run_gemm(x, w, nullptr, nullptr, A, lda, CONVROT_ACT_NONE, dev_status, stream);
 }
 
+convrot_status convrot_wait_check(int32_t *dev_status, uint64_t limit_ns, int32_t arrive, cudaStream_t stream)
+{
+    if (!dev_status || limit_ns == 0 || limit_ns > CONVROT_WAIT_LIMIT_NS) return CONVROT_ERR_INVALID_ARG;
+    return convrot::launch_wait_check(dev_status, limit_ns, arrive, stream) == cudaSuccess ? CONVROT_OK
+                                                                                           : CONVROT_ERR_CUDA;
+}
+
 const char *convrot_status_string(convrot_status s)
 {
     switch (s) {

@@ -56,6 +56,10 @@ cudaError_t launch_lora_prepare_down(const float *A, int32_t r, int32_t k, int64
 cudaError_t launch_lora_down(const float *X, int64_t m, int32_t k, int64_t ldx, const float *A_ext, int32_t r,
                              int64_t lda, void *t, int64_t ldt, int32_t *dev_status, cudaStream_t stream);
 
+// One CTA waiting on an mbarrier through the kernels' bounded wait (arrive = 0:
+// nothing arrives and it reports CONVROT_ERR_TIMEOUT after limit_ns).
+cudaError_t launch_wait_check(int32_t *dev_status, uint64_t limit_ns, int arrive, cudaStream_t stream);
+
 // GELU, erf or tanh form (convrot_activation), on the epilogue's fp32 value.
 // The tanh form is evaluated through its exact identity
 // 0.5 v (1 + tanh(u)) = v / (1 + e^(-2u)), u = sqrt(2/pi) (v + 0.044715 v^3):

@@ -46,6 +46,7 @@
 
 #include "../../include/convrot.h"
 #include "internal.h"
+#include "tc_common.cuh"
 
 namespace convrot {
 namespace {
@@ -552,39 +553,7 @@ struct RingPlan {
     uint32_t stage_bytes;  // rows_per_stage * row_bytes
 };
 
-__device__ __forceinline__ uint64_t globaltimer()
-{
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-constexpr uint64_t kTimeoutNs = 4000000000ull;  // 4 s
-
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
-{
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer();
-    for (;;) {
-#pragma unroll 1
-        for (int i = 0; i < 32; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
-        if (globaltimer() - t0 > kTimeoutNs) return false;
-    }
-}
+using tc::mbar_wait;
 
 template <int N, bool kBf16>
 __global__ void __launch_bounds__(512) pack_ring_kernel(PackArgs a, RingPlan P)

@@ -9,10 +9,12 @@
 #include <cstdint>
 #include <mutex>
 
+#include "../../include/convrot.h"
+
 namespace convrot {
 namespace tc {
 
-constexpr uint64_t kTimeoutNs = 4000000000ull;  // 4 s
+constexpr uint64_t kTimeoutNs = CONVROT_WAIT_LIMIT_NS;  // 4 s
 
 __device__ __forceinline__ uint64_t globaltimer()
 {
@@ -39,8 +41,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
-// Waits for the phase with the given parity; false if it did not come within the limit.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
+// Waits for the phase with the given parity; false if it did not come within
+// limit_ns of the first failed try.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns = kTimeoutNs)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
@@ -48,7 +51,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
 #pragma unroll 1
         for (int i = 0; i < 32; ++i)
             if (mbar_try_wait(bar, parity)) return true;
-        if (globaltimer() - t0 > kTimeoutNs) return false;
+        if (globaltimer() - t0 > limit_ns) return false;
     }
 }
 

@@ -195,3 +195,10 @@ def test_linear_lora_validates(lib):
     assert call(x, w, t=None) == cr.ERR_INVALID_ARG
     xi, wi = pair(codes=cr.CODES_I8)
     assert call(xi, wi) == cr.ERR_UNSUPPORTED
+
+
+def test_wait_check_validates_before_launching(lib):
+    assert lib.convrot_wait_check(None, 1000, 0, None) == cr.ERR_INVALID_ARG
+    assert lib.convrot_wait_check(FAKE, 0, 0, None) == cr.ERR_INVALID_ARG
+    assert lib.convrot_wait_check(FAKE, cr.WAIT_LIMIT_NS + 1, 0, None) == cr.ERR_INVALID_ARG
+    assert "bounded wait" in cr.status_string(cr.ERR_TIMEOUT)
