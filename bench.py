@@ -90,10 +90,13 @@ def measured_traffic(workload: str, codes: str):
     entry = json.load(open(tpath)).get(f"{workload}/{codes}")
     if not entry:
         return None
-    src = os.path.join(ROOT, entry["source"])
-    if not os.path.exists(src):
-        return None
-    if hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] != entry["sha256_16"]:
+    h = hashlib.sha256()
+    for rel in entry["sources"]:  # the kernel's file and the headers it is built from, in order
+        src = os.path.join(ROOT, rel)
+        if not os.path.exists(src):
+            return None
+        h.update(open(src, "rb").read())
+    if h.hexdigest()[:16] != entry["sha256_16"]:
         return None
     return entry["gemm_bytes"]
 
