@@ -43,6 +43,8 @@ def parse():
     ap.add_argument("--workload", default="mlp_up")
     ap.add_argument("--codes", choices=["auto", "i8", "bf16"], default="auto")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--eager", action="store_true",
+                    help="launch the timed steps one call at a time instead of replaying them as one CUDA graph")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="approximate CPU time budget of the oracle baseline sample")
     return ap.parse_args()
@@ -271,7 +273,9 @@ def run_ours(args):
         Ys.append([torch.empty((wl.m, st.n), dtype=torch.float32, device=dev) for _ in range(R)])
         del Ws
     n_out = stages[-1].n
-    stream = torch.cuda.current_stream(dev)
+    # a stream of its own: the timed steps are captured into a CUDA graph on it
+    stream = torch.cuda.Stream(dev)
+    torch.cuda.synchronize(dev)
     if wl.lora_r:  # runtime LoRA on the first linear: T from the unrotated X, one extra GEMM chunk
         A_l, B_l = inputs.lora_weights(wl)
         A_l = cr.convrot_lora_prepare_down(torch.from_numpy(A_l).to(dev))
@@ -318,6 +322,18 @@ def run_ours(args):
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize(dev)
+    # The K timed steps as one CUDA graph: the same kernels on the same buffers,
+    # launched without the host between them. Replayed once untimed so that the
+    # graph's upload is not in the timed region.
+    graph = None
+    if not args.eager:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for i in range(args.steps):
+                step(i)
+        with torch.cuda.stream(stream):  # replay() launches on the current stream
+            graph.replay()
+        torch.cuda.synchronize(dev)
     if pg:
         pg.barrier()
     torch.cuda.synchronize(dev)
@@ -335,16 +351,25 @@ def run_ours(args):
     evs = [[[None, torch.cuda.Event(enable_timing=True)] for _ in range(n_marks)] for _ in range(args.steps)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
-    # the timed loop runs several times over so the clock sampler sees a loaded GPU
+    # The timed region holds no events between kernels: each one serialises the
+    # stream (~2 us), so the per-kernel durations come from a second pass over
+    # the same K steps with an event at every kernel boundary.
     t_start.record(stream)
-    for i in range(args.steps):
-        step(i, evs[i])
+    if graph is not None:
+        with torch.cuda.stream(stream):
+            graph.replay()
+    else:
+        for i in range(args.steps):
+            step(i)
     t_end.record(stream)
     torch.cuda.synchronize(dev)
     if pg:
         pg.barrier()
     torch.cuda.synchronize(dev)
     total_ms = t_start.elapsed_time(t_end)
+    for i in range(args.steps):
+        step(i, evs[i])
+    torch.cuda.synchronize(dev)
     pack_ms = [kernel_ms(e, "pack") for e in evs]
     gemm_ms = [kernel_ms(e, "gemm") for e in evs]
     lora_ms = [kernel_ms(e, "lora_down") for e in evs] if wl.lora_r else None
@@ -424,7 +449,11 @@ def run_ours(args):
         "config": {"workload": workload_name(wl), "global_batch": wl.m * world,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "codes": "i8" if codes == cr.CODES_I8 else "bf16",
-                   "l2": f"{R} rotating input/output sets, {touched / 1e6:.0f} MB touched per step (> L2)"},
+                   "l2": f"{R} rotating input/output sets, {touched / 1e6:.0f} MB touched per step (> L2)",
+                   "launch": ("eager, one C-ABI call per kernel" if graph is None else
+                              "the K timed steps replayed as one CUDA graph of the same C-ABI launches"),
+                   "kernel_timing": "CUDA events at every kernel boundary, in a second pass over the same K "
+                                    "steps (pack_ms, gemm_ms and the rooflines come from it)"},
         "pack_gbs": pack_gbs, "pack_ms": pack_avg, "gemm_ms": gemm_avg, "gemm_tops": gemm_tops,
         **({"lora_down_ms": sum(lora_ms) / len(lora_ms),
             "lora": f"rank {wl.lora_r}, scale {wl.lora_scale:g}: T = X A^T in its own kernel (lora_down_ms), "

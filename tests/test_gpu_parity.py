@@ -383,6 +383,54 @@ def test_full_size_attention_grouped_qkv():
                               (codes_np(pw), Qw_ref), px.scale.cpu().numpy()[rows], pw.scale.cpu().numpy())
 
 
+def test_graph_replay_equals_eager_steps():
+    """bench.py times its steps as one captured CUDA graph of the same C-ABI
+    launches. Replaying it (pack, LoRA down, the LoRA linear with GELU, then
+    the down-projection's pack and linear, on two rotating buffer sets) gives
+    bit for bit what the eager calls give, and the status word stays clear."""
+    rng = np.random.default_rng(31)
+    m, k, n, r = 300, 512, 768, 32
+    Xs = [to_dev(special_rows(rng, m, k)) for _ in range(2)]
+    W1 = to_dev((0.02 * rng.standard_normal((n, k))).astype(np.float32))
+    W2 = to_dev((0.02 * rng.standard_normal((k, n))).astype(np.float32))
+    b1, b2 = to_dev(rng.standard_normal(n).astype(np.float32)), to_dev(rng.standard_normal(k).astype(np.float32))
+    pw1, pw2 = cr.convrot_quantize_weights(W1, 64, cr.CODES_BF16), cr.convrot_quantize_weights(W2, 256, cr.CODES_BF16)
+    A_ext = cr.convrot_lora_prepare_down(to_dev((0.05 * rng.standard_normal((r, k))).astype(np.float32)))
+    B_ext = cr.convrot_lora_prepare(to_dev((0.05 * rng.standard_normal((n, r))).astype(np.float32)), 2.0)
+    px1 = [cr.empty_packed(m, k, cr.CODES_BF16, "cuda") for _ in range(2)]
+    px2 = [cr.empty_packed(m, n, cr.CODES_BF16, "cuda") for _ in range(2)]
+    T = [torch.empty((m, cr.lora_cols(r)), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    H = [torch.empty((m, n), device="cuda") for _ in range(2)]
+    Y = [torch.empty((m, k), device="cuda") for _ in range(2)]
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+
+    def step(j):
+        cr.convrot_lora_down(Xs[j], A_ext, out=T[j], dev_status=st, stream=s)
+        cr.convrot_pack_activations(Xs[j], 64, cr.CODES_BF16, out=px1[j], dev_status=st, stream=s)
+        cr.convrot_linear_lora(px1[j], pw1, b1, cr.ACT_GELU_TANH, T[j], B_ext, r, out=H[j], dev_status=st, stream=s)
+        cr.convrot_pack_activations(H[j], 256, cr.CODES_BF16, out=px2[j], dev_status=st, stream=s)
+        cr.convrot_linear_act(px2[j], pw2, b2, cr.ACT_NONE, out=Y[j], dev_status=st, stream=s)
+
+    with torch.cuda.stream(s):
+        for j in range(2):
+            step(j)
+    torch.cuda.synchronize()
+    eager = [y.clone() for y in Y] + [h.clone() for h in H]
+    for t in Y + H:
+        t.fill_(float("nan"))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for j in range(2):
+            step(j)
+    g.replay()
+    torch.cuda.synchronize()
+    for a, b in zip(eager, Y + H):
+        assert torch.equal(a, b)
+    assert int(st.item()) == cr.OK
+
+
 # ---- runtime LoRA side branch
 
 @pytest.mark.parametrize("m,k,r", [(300, 512, 16), (129, 3072, 64), (64, 200, 48), (1000, 1024, 256)])
