@@ -282,42 +282,34 @@ def run_ours(args):
         B_ext = cr.convrot_lora_prepare(torch.from_numpy(B_l).to(dev), wl.lora_scale)
         T_ext = [torch.empty((wl.m, cr.lora_cols(wl.lora_r)), dtype=torch.bfloat16, device=dev) for _ in range(R)]
 
-    def run_stages(x_in, j, marks=None):
-        """One step; with marks (a list of (tag, event) slots) it records an event before
-        each kernel, tagged with the kernel, and one at the end."""
-        used = 0
-
-        def mark(tag):
-            nonlocal used
-            if marks is not None:
-                marks[used][1].record(stream)
-                marks[used][0] = tag
-                used += 1
-
+    def step_ops(x_in, j):
+        """One step as its kernel launches, in order: (tag, launch) pairs."""
+        ops = []
         h = x_in
         for s_i, st in enumerate(stages):
+            def pack(h=h, s_i=s_i):
+                cr.convrot_pack_activations(h, wl.G, codes, out=pxs[s_i][j], stream=stream)
             if wl.lora_r and s_i == 0:
-                mark("lora_down")
-                cr.convrot_lora_down(h, A_l, out=T_ext[j], stream=stream)
-            mark("pack")
-            cr.convrot_pack_activations(h, wl.G, codes, out=pxs[s_i][j], stream=stream)
-            mark("gemm")
-            if wl.lora_r and s_i == 0:
-                cr.convrot_linear_lora(pxs[s_i][j], pws[s_i][j], biases[s_i], st.act, T_ext[j], B_ext, wl.lora_r,
-                                       out=Ys[s_i][j], stream=stream)
+                ops.append(("lora_down", lambda h=h: cr.convrot_lora_down(h, A_l, out=T_ext[j], stream=stream)))
+                ops.append(("pack", pack))
+                ops.append(("gemm", lambda s_i=s_i, st=st: cr.convrot_linear_lora(
+                    pxs[s_i][j], pws[s_i][j], biases[s_i], st.act, T_ext[j], B_ext, wl.lora_r, out=Ys[s_i][j],
+                    stream=stream)))
             else:
-                cr.convrot_linear_act(pxs[s_i][j], pws[s_i][j], biases[s_i], st.act, out=Ys[s_i][j],
-                                      stream=stream)
+                ops.append(("pack", pack))
+                ops.append(("gemm", lambda s_i=s_i, st=st: cr.convrot_linear_act(
+                    pxs[s_i][j], pws[s_i][j], biases[s_i], st.act, out=Ys[s_i][j], stream=stream)))
             h = Ys[s_i][j]
-        mark("end")
-        return h
+        return ops, h
 
-    def step(i, marks=None):
-        run_stages(Xs[i % R], i % R, marks)
+    def run_stages(x_in, j):
+        ops, y = step_ops(x_in, j)
+        for _, launch in ops:
+            launch()
+        return y
 
-    def kernel_ms(marks, tag):
-        """Milliseconds between each event tagged `tag` and the next event, summed."""
-        return sum(marks[i][1].elapsed_time(marks[i + 1][1]) for i in range(len(marks) - 1) if marks[i][0] == tag)
+    def step(i):
+        run_stages(Xs[i % R], i % R)
 
     for i in range(args.warmup):
         step(i)
@@ -347,13 +339,10 @@ def run_ours(args):
     clocks = ClockSampler(uuid)
     clocks.start()
     time.sleep(0.3)
-    n_marks = 2 * len(stages) + (1 if wl.lora_r else 0) + 1
-    evs = [[[None, torch.cuda.Event(enable_timing=True)] for _ in range(n_marks)] for _ in range(args.steps)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     # The timed region holds no events between kernels: each one serialises the
-    # stream (~2 us), so the per-kernel durations come from a second pass over
-    # the same K steps with an event at every kernel boundary.
+    # stream (~2.4 us), so the per-kernel durations are measured apart (below).
     t_start.record(stream)
     if graph is not None:
         with torch.cuda.stream(stream):
@@ -367,12 +356,39 @@ def run_ours(args):
         pg.barrier()
     torch.cuda.synchronize(dev)
     total_ms = t_start.elapsed_time(t_end)
-    for i in range(args.steps):
-        step(i, evs[i])
-    torch.cuda.synchronize(dev)
-    pack_ms = [kernel_ms(e, "pack") for e in evs]
-    gemm_ms = [kernel_ms(e, "gemm") for e in evs]
-    lora_ms = [kernel_ms(e, "lora_down") for e in evs] if wl.lora_r else None
+    # Per-kernel durations: each launch of the step repeated K times back to back
+    # over the rotating sets (as one CUDA graph unless --eager), with an event
+    # pair around the batch: its average launch duration, free of the stream
+    # serialisation that an event between two kernels costs.
+    kern_ms = {}
+    n_ops = len(step_ops(Xs[0], 0)[0])
+    for q in range(n_ops):
+        tag = step_ops(Xs[0], 0)[0][q][0]
+
+        def batch(q=q):
+            for i in range(args.steps):
+                step_ops(Xs[i % R], i % R)[0][q][1]()
+        g = None
+        if graph is not None:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                batch()
+            with torch.cuda.stream(stream):
+                g.replay()
+        else:
+            batch()
+        torch.cuda.synchronize(dev)
+        b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        b0.record(stream)
+        if g is not None:
+            with torch.cuda.stream(stream):
+                g.replay()
+        else:
+            batch()
+        b1.record(stream)
+        torch.cuda.synchronize(dev)
+        kern_ms[tag] = kern_ms.get(tag, 0.0) + b0.elapsed_time(b1) / args.steps
+        del g
     # keep the GPU busy a little longer with the same steps for the clock record
     t_keep = time.time()
     i = 0
@@ -431,8 +447,8 @@ def run_ours(args):
 
     ops = float(wl.step_ops)
     value = job_tops(world, ops, ms_step)
-    gemm_avg = sum(gemm_ms) / len(gemm_ms)
-    pack_avg = sum(pack_ms) / len(pack_ms)
+    gemm_avg = kern_ms["gemm"]
+    pack_avg = kern_ms["pack"]
     pk = peaks()
     gemm_tops = ops / (gemm_avg * 1e-3) / 1e12
     pack_bytes = sum(wl.m * (4 * st.k + code_b * st.k + 4) for st in stages)
@@ -452,10 +468,10 @@ def run_ours(args):
                    "l2": f"{R} rotating input/output sets, {touched / 1e6:.0f} MB touched per step (> L2)",
                    "launch": ("eager, one C-ABI call per kernel" if graph is None else
                               "the K timed steps replayed as one CUDA graph of the same C-ABI launches"),
-                   "kernel_timing": "CUDA events at every kernel boundary, in a second pass over the same K "
-                                    "steps (pack_ms, gemm_ms and the rooflines come from it)"},
+                   "kernel_timing": "each launch of the step repeated K times back to back over the rotating "
+                                    "sets, CUDA events around the batch (pack_ms, gemm_ms and the rooflines)"},
         "pack_gbs": pack_gbs, "pack_ms": pack_avg, "gemm_ms": gemm_avg, "gemm_tops": gemm_tops,
-        **({"lora_down_ms": sum(lora_ms) / len(lora_ms),
+        **({"lora_down_ms": kern_ms["lora_down"],
             "lora": f"rank {wl.lora_r}, scale {wl.lora_scale:g}: T = X A^T in its own kernel (lora_down_ms), "
                     "the correction as an extra fp32 chunk of the GEMM (in gemm_ms); its own "
                     "multiply-adds are not counted in value"} if wl.lora_r else {}),
