@@ -137,23 +137,24 @@ __device__ __forceinline__ void act_box(uint32_t buf, int lane)
 
 // With kLora, lora_taddr is the TMEM address of this warp's rows and columns
 // of the LoRA chunk (fp32), added to each output before the activation.
-template <bool kRawInt32, int kAct, bool kLora = false>
+// NACC: columns per warp (128 or 64); NBUF: the warp's staging buffers (2 or 1).
+template <bool kRawInt32, int kAct, bool kLora = false, int NACC = 128, int NBUF = 2>
 __device__ __forceinline__ void store_tile_rows(const TcParams &p, const CUtensorMap *tmY, uint32_t out_smem,
                                                 uint32_t &store_iter, int64_t row0, int64_t col0,
-                                                const int32_t (&acc)[128], int lane, int ncols = 128,
+                                                const int32_t (&acc)[NACC], int lane, int ncols = NACC,
                                                 uint32_t lora_taddr = 0)
 {
     const int64_t row = row0 + lane;
     float sxr = 0.0f;
     if constexpr (!kRawInt32) sxr = row < p.m ? p.sx[row] : 0.0f;
 #pragma unroll
-    for (int cc = 0; cc < 4; ++cc) {
+    for (int cc = 0; cc < NACC / 32; ++cc) {
         if (cc * 32 >= ncols) break;
         const int64_t x = col0 + cc * 32;
         if (x >= p.n) break;
         if ((kAct != 0 || kLora) && x + 32 > p.n) {
             // ragged last box with an activation or a LoRA term: stage, activate, then masked stores
-            const uint32_t buf = out_smem + (store_iter & 1u) * OUT_BUF_BYTES;
+            const uint32_t buf = out_smem + (NBUF == 2 ? (store_iter & 1u) * OUT_BUF_BYTES : 0u);
             if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
             __syncwarp();
 #pragma unroll
@@ -202,8 +203,13 @@ __device__ __forceinline__ void store_tile_rows(const TcParams &p, const CUtenso
             }
             continue;
         }
-        const uint32_t buf = out_smem + (store_iter & 1u) * OUT_BUF_BYTES;
-        if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+        const uint32_t buf = out_smem + (NBUF == 2 ? (store_iter & 1u) * OUT_BUF_BYTES : 0u);
+        if (lane == 0) {
+            if constexpr (NBUF == 2)
+                asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+            else
+                asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+        }
         __syncwarp();
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
@@ -549,11 +555,25 @@ __device__ __forceinline__ void arrive_remote(uint32_t cluster_bar)
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
 }
 
+// Warp roles of the pair kernel: warpgroup 0 holds the TMA producer (warp 0),
+// the MMA issuer (warp 1) and two idle warps; warpgroups 1-4 are sixteen
+// epilogue warps, four per TMEM lane quadrant, each draining 32 rows x 64
+// columns. Launched at 96 registers a thread (five warps on some SM
+// sub-partitions: 16 K registers / (5 x 32) = 102, rounded down to 8s),
+// warpgroup 0 gives registers back and the epilogue warps take them:
+// 4 x 32 x 40 + 16 x 32 x 104 = 58368 <= 640 x 96 = 61440.
+constexpr int PAIR_EPI_WARPS = 16;
+constexpr int PAIR_THREADS = 128 + PAIR_EPI_WARPS * 32;
+constexpr int PAIR_COLS = 64;  // columns per epilogue warp
+constexpr int kRegsWg0 = 40, kRegsEpi = 104;
+static_assert(4 * 32 * kRegsWg0 + PAIR_EPI_WARPS * 32 * kRegsEpi <= PAIR_THREADS * 96, "register split");
+static_assert(PAIR_EPI_WARPS * OUT_BUF_BYTES <= OUT_BYTES, "one staging box per epilogue warp");
+
 // kLora: after each tile's K slices, the producer streams lora_kst more slices
 // from tmLa (T_ext rows) and tmLb (B_ext rows); the MMA runs them as one extra
 // chunk whose fp32 sums are not promoted to int32 but added to the output.
 template <int BN, bool kRawInt32, int kAct, bool kLora>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
     gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmLa,
                         const __grid_constant__ CUtensorMap tmLb, TcParams p)
@@ -591,7 +611,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(accf_bar(b), 1);
-            mbar_init(acce_bar(b), 2 * EPI_WARPS);
+            mbar_init(acce_bar(b), 2 * PAIR_EPI_WARPS);
         }
         if constexpr (kLora) {
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmLa)) : "memory");
@@ -621,7 +641,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         if (p.dev_status) atomicExch(p.dev_status, static_cast<int32_t>(CONVROT_ERR_TIMEOUT));
     };
 
-    if (warp == 0) {
+    if (warp < 4) {
+      // warpgroup 0: every warp runs this one instruction, then the roles split
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsWg0));
+      if (warp == 0) {
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
@@ -711,20 +734,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             mbar_wait(done_bar, 0);
         }
         __syncwarp();
+      }
     } else {
-        const int q = warp & 3;
-        const int h = (warp - 2) >> 2;
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsEpi));
+        const int q = warp & 3;            // TMEM lane quadrant (warp % 4)
+        const int part = (warp - 4) >> 2;  // 64-column slice of the tile
+        const int ncols = BNP - part * PAIR_COLS < PAIR_COLS ? (BNP - part * PAIR_COLS > 0 ? BNP - part * PAIR_COLS : 0)
+                                                             : PAIR_COLS;
         const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
-        const uint32_t out_smem = out_base + (warp - 2) * OUT_WARP_BYTES;
+        const uint32_t out_smem = out_base + (warp - 4) * OUT_BUF_BYTES;
         uint32_t store_iter = 0;
         uint32_t chunk_iter = 0;
         bool ok = true;
         for (int64_t t = pair_id; t < n_tiles && ok; t += n_pairs) {
             int64_t mt, nt;
             tile_coords(t, n_mt, n_nt, mt, nt);
-            int32_t acc[128];
+            int32_t acc[PAIR_COLS];
 #pragma unroll
-            for (int i = 0; i < 128; ++i) acc[i] = 0;
+            for (int i = 0; i < PAIR_COLS; ++i) acc[i] = 0;
             for (int c = 0; c < n_chunks; ++c, ++chunk_iter) {
                 const uint32_t buf = chunk_iter & 1u;
                 if (*abort_flag || !mbar_wait(accf_bar(buf), (chunk_iter >> 1) & 1u)) {
@@ -732,10 +759,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t taddr = tmem_base + lane_off + buf * BNP + h * 128;
+                const uint32_t taddr = tmem_base + lane_off + buf * BNP + part * PAIR_COLS;
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    if (h * 128 + j * 32 >= BNP) break;  // the second half is BN - 128 columns wide
+                for (int j = 0; j < PAIR_COLS / 32; ++j) {
+                    if (j * 32 >= ncols) break;  // the last slice is narrower when BN is not a multiple of 64
                     uint32_t r[32];
                     tmem_ld32(taddr + j * 32, r);
 #pragma unroll
@@ -754,17 +781,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                 }
                 tc_fence_after();
                 // the LoRA chunk stays in tensor memory until the store reads it box by box
-                store_tile_rows<kRawInt32, kAct, true>(
+                store_tile_rows<kRawInt32, kAct, true, PAIR_COLS, 1>(
                     p, &tmY, out_smem, store_iter, mt * 2 * BMC + static_cast<int64_t>(rank) * BMC + q * 32,
-                    nt * BNP + h * 128, acc, lane, h == 0 ? 128 : BNP - 128, tmem_base + lane_off + buf * BNP + h * 128);
+                    nt * BNP + part * PAIR_COLS, acc, lane, ncols, tmem_base + lane_off + buf * BNP + part * PAIR_COLS);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) arrive_remote(map_to_rank(acce_bar(buf), 0));
                 ++chunk_iter;
             } else {
-                store_tile_rows<kRawInt32, kAct>(p, &tmY, out_smem, store_iter,
-                                                 mt * 2 * BMC + static_cast<int64_t>(rank) * BMC + q * 32,
-                                                 nt * BNP + h * 128, acc, lane, h == 0 ? 128 : BNP - 128);
+                store_tile_rows<kRawInt32, kAct, false, PAIR_COLS, 1>(
+                    p, &tmY, out_smem, store_iter, mt * 2 * BMC + static_cast<int64_t>(rank) * BMC + q * 32,
+                    nt * BNP + part * PAIR_COLS, acc, lane, ncols);
             }
         }
         drain_stores(lane);
@@ -832,7 +859,7 @@ cudaError_t launch_pair(const GemmArgs &g, TcParams p, const CUtensorMap &ty, in
     auto run = [&](auto kern) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
         if (e != cudaSuccess) return e;
-        kern<<<grid, THREADS, C::SMEM_BYTES, stream>>>(pa, pb, ty, la, lb, p);
+        kern<<<grid, pair::PAIR_THREADS, C::SMEM_BYTES, stream>>>(pa, pb, ty, la, lb, p);
         return cudaGetLastError();
     };
     if (g.a) return run(pair::gemm_tc_pair_kernel<BN, true, 0, false>);
