@@ -16,15 +16,22 @@
 // register accumulators. The result equals the page's signed 32-bit
 // accumulation bit for bit.
 //
-// Structure (one CTA per SM, persistent over 128 x 256 output tiles):
-//   warp 0      TMA producer: 64-wide K slices of A (128 rows) and B (256
-//               rows), 128-byte swizzled, into a 4-stage shared-memory ring.
-//   warp 1      allocates 512 TMEM columns (two 128 x 256 fp32 buffers) and
-//               issues tcgen05.mma (M = 128, N = 256, K = 16) from one thread.
-//   warps 2-9   epilogue: drain each finished chunk from TMEM (tcgen05.ld),
-//               accumulate in int32, and after the last chunk of a tile write
-//               Y (or the raw int32 A) while the MMA warp runs the next chunk
-//               into the other TMEM buffer.
+// Main form, gemm_tc_pair_kernel (m > 128): a CTA pair (cluster of 2,
+// tcgen05 cta_group::2), persistent over 256 x 256 output tiles.
+//   warp 0      TMA producer of each CTA: 64-wide K slices of its 128 rows of
+//               A and 128 rows of B, 128-byte swizzled, into a 5-stage ring;
+//               both CTAs' copies complete on the even CTA's barrier.
+//   warp 1      allocates 512 TMEM columns (two 128 x 256 fp32 buffers per
+//               CTA); in the even CTA one thread issues tcgen05.mma (M = 256,
+//               N = 256, K = 16) over both CTAs' shared memory.
+//   warps 4-19  epilogue, sixteen warps (four per TMEM lane quadrant, 32 rows
+//               x 64 columns each): drain each finished chunk from TMEM
+//               (tcgen05.ld), accumulate in int32, and after the last chunk of
+//               a tile write Y (or the raw int32 A) while the MMA warp runs the
+//               next chunk into the other TMEM buffer.
+// Single-CTA form, gemm_tc_kernel (m <= 128), persistent over 128 x 256
+// tiles: warp 0 produces into a 3-stage ring, warp 1 issues M = 128 MMAs,
+// warps 2-9 are the epilogue (32 rows x 128 columns each).
 // Every mbarrier wait is bounded: a wait that runs out writes
 // CONVROT_ERR_TIMEOUT to the caller's status word and the CTA winds down
 // (in-flight copies and MMAs are waited for, TMEM is freed).
@@ -109,14 +116,14 @@ struct TcParams {
 };
 
 
-// One epilogue warp's 32 rows x 128 columns of the tile (lane i holds row
+// One epilogue warp's 32 rows x NACC columns of the tile (lane i holds row
 // row0 + i in acc[]): raw int32 A, or Y = float(A) * s_x[row] * s_w[col] +
-// b[col]. Each 32 x 32 box is written to one of the warp's two shared-memory
+// b[col]. Each 32 x 32 box is written to one of the warp's NBUF shared-memory
 // buffers in the 128-byte-swizzled layout (16-byte chunk c of row r at c ^
 // (r & 7): conflict-free for the row-per-lane writes) and stored by TMA, which
 // writes whole lines and clips rows >= m. A box that would cross column n is
 // written directly with masked stores instead. A buffer is reused only after
-// the store issued from it two boxes earlier has read it.
+// the store issued from it NBUF boxes earlier has read it.
 // Activation over the warp's staged 32 x 32 box (lane i owns row i), in a
 // loop unrolled only twice so that the accumulators of the boxes still to
 // come stay in registers while it runs (fully unrolled, the GELU's
