@@ -113,6 +113,11 @@ struct TcParams {
     int32_t *dev_status;
     int32_t act;       // convrot_activation on Y
     int32_t lora_kst;  // 64-wide K slices of the LoRA operands (pair kernel, kLora)
+    // pair kernel: tiles [0, full_tiles) run as whole tiles, full_tiles a
+    // multiple of the pairs; each tile past them (the last, partial wave) is
+    // split along N into tail_split items (1, 2, 4 or 8)
+    int64_t full_tiles;
+    int32_t tail_split;
 };
 
 
@@ -583,7 +588,8 @@ template <int BN, bool kRawInt32, int kAct, bool kLora>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
     gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmLa,
-                        const __grid_constant__ CUtensorMap tmLb, TcParams p)
+                        const __grid_constant__ CUtensorMap tmLb, const __grid_constant__ CUtensorMap tmBt,
+                        TcParams p)
 {
     using C = Cfg<BN>;
     constexpr int STAGES = C::STAGES, STAGE_BYTES = C::STAGE_BYTES, A_BYTES = C::A_BYTES, BNP = C::BNP, BNC = C::BNC;
@@ -657,29 +663,44 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
             uint32_t phase = 0;
             int issued = 0;
             bool ok = true;
-            for (int64_t t = pair_id; t < n_tiles && ok; t += n_pairs) {
-                int64_t mt64, nt64;
-                tile_coords(t, n_mt, n_nt, mt64, nt64);
-                const int mt = static_cast<int>(mt64), nt = static_cast<int>(nt64);
+            // one tile or item: every K slice of its A rows and of this CTA's brow.. B rows
+            auto produce = [&](int mt, int brow, uint32_t tx, const CUtensorMap *bmap) {
                 const int arow = mt * 2 * BMC + static_cast<int>(rank) * BMC;
-                const int brow = nt * BNP + static_cast<int>(rank) * BNC;
                 for (int ks = 0; ks < kst + lkst; ++ks) {
                     if (*abort_flag || !mbar_wait(empty_bar(stage), phase ^ 1u)) {
                         ok = false;
-                        break;
+                        return;
                     }
                     const uint32_t sa = base + stage * STAGE_BYTES;
-                    if (leader) mbar_arrive_expect_tx(full_bar(stage), 2 * STAGE_BYTES);
+                    if (leader) mbar_arrive_expect_tx(full_bar(stage), tx);
                     const uint32_t lbar = map_to_rank(full_bar(stage), 0);
                     const bool lo = kLora && ks >= kst;
                     const int kx = (lo ? ks - kst : ks) * BK;
                     tma_load_2d_pair(sa, lo ? &tmLa : &tmA, kx, arow, lbar);
-                    tma_load_2d_pair(sa + A_BYTES, lo ? &tmLb : &tmB, kx, brow, lbar);
+                    tma_load_2d_pair(sa + A_BYTES, lo ? &tmLb : bmap, kx, brow, lbar);
                     ++issued;
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
+                }
+            };
+            for (int64_t t = pair_id; t < p.full_tiles && ok; t += n_pairs) {
+                int64_t mt64, nt64;
+                tile_coords(t, n_mt, n_nt, mt64, nt64);
+                produce(static_cast<int>(mt64), static_cast<int>(nt64) * BNP + static_cast<int>(rank) * BNC,
+                        2u * STAGE_BYTES, &tmB);
+            }
+            {  // the last, partial wave: its tiles split along N into items
+                const int sp = p.tail_split, wd = BNP / sp;
+                const int64_t n_items = (n_tiles - p.full_tiles) * sp;
+                for (int64_t u = pair_id; u < n_items && ok; u += n_pairs) {
+                    int64_t mt64, nt64;
+                    tile_coords(p.full_tiles + u / sp, n_mt, n_nt, mt64, nt64);
+                    const int brow = static_cast<int>(nt64) * BNP + static_cast<int>(u % sp) * wd +
+                                     static_cast<int>(rank) * (wd / 2);
+                    produce(static_cast<int>(mt64), brow, 2u * static_cast<uint32_t>(A_BYTES + (wd / 2) * BK * 2),
+                            sp > 1 ? &tmBt : &tmB);
                 }
             }
             if (!ok) {
@@ -703,12 +724,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
             uint32_t phase = 0;
             uint32_t chunk_iter = 0;
             bool ok = true;
-            for (int64_t t = pair_id; t < n_tiles && ok; t += n_pairs) {
+            // one tile or item; idesc carries its width as the instruction's N
+            auto mma_tile = [&](uint32_t idesc) {
                 for (int c = 0; c < n_chunks + (kLora ? 1 : 0) && ok; ++c, ++chunk_iter) {
                     const uint32_t buf = chunk_iter & 1u;
                     if (*abort_flag || !mbar_wait(acce_bar(buf), ((chunk_iter >> 1) & 1u) ^ 1u)) {
                         ok = false;
-                        break;
+                        return;
                     }
                     tc_fence_after();
                     const uint32_t d_tmem = tmem_base + buf * BNP;
@@ -718,23 +740,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
                     for (int ks = ks0; ks < ks1; ++ks) {
                         if (*abort_flag || !mbar_wait(full_bar(stage), phase)) {
                             ok = false;
-                            break;
+                            return;
                         }
                         tc_fence_after();
                         const uint32_t sa = base + stage * STAGE_BYTES;
                         const uint64_t da = smem_desc(sa), db = smem_desc(sa + A_BYTES);
 #pragma unroll
                         for (int kk = 0; kk < BK / UMMA_K; ++kk)
-                            mma_pair(d_tmem, da + 2u * kk, db + 2u * kk, C::kIdesc, (ks > ks0 || kk > 0) ? 1u : 0u);
+                            mma_pair(d_tmem, da + 2u * kk, db + 2u * kk, idesc, (ks > ks0 || kk > 0) ? 1u : 0u);
                         commit_both(empty_bar(stage));  // frees this stage in both CTAs once the MMAs finish
                         if (++stage == STAGES) {
                             stage = 0;
                             phase ^= 1u;
                         }
                     }
-                    if (!ok) break;
                     commit_both(accf_bar(buf));
                 }
+            };
+            for (int64_t t = pair_id; t < p.full_tiles && ok; t += n_pairs) mma_tile(C::kIdesc);
+            {
+                const int sp = p.tail_split;
+                const int64_t n_items = (n_tiles - p.full_tiles) * sp;
+                const uint32_t idesc = (C::kIdesc & ~(0x3Fu << 17)) | (static_cast<uint32_t>((BNP / sp) >> 3) << 17);
+                for (int64_t u = pair_id; u < n_items && ok; u += n_pairs) mma_tile(idesc);
             }
             if (!ok) fail();
             commit_local(done_bar);
@@ -745,15 +773,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsEpi));
         const int q = warp & 3;            // TMEM lane quadrant (warp % 4)
-        const int part = (warp - 4) >> 2;  // 64-column slice of the tile
-        const int ncols = BNP - part * PAIR_COLS < PAIR_COLS ? (BNP - part * PAIR_COLS > 0 ? BNP - part * PAIR_COLS : 0)
-                                                             : PAIR_COLS;
+        const int part = (warp - 4) >> 2;  // 64-column slice of the tile or item
         const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
         const uint32_t out_smem = out_base + (warp - 4) * OUT_BUF_BYTES;
         uint32_t store_iter = 0;
         uint32_t chunk_iter = 0;
         bool ok = true;
-        for (int64_t t = pair_id; t < n_tiles && ok; t += n_pairs) {
+        const int ncols = BNP - part * PAIR_COLS < PAIR_COLS ? (BNP - part * PAIR_COLS > 0 ? BNP - part * PAIR_COLS : 0)
+                                                             : PAIR_COLS;
+        for (int64_t t = pair_id; t < p.full_tiles && ok; t += n_pairs) {
             int64_t mt, nt;
             tile_coords(t, n_mt, n_nt, mt, nt);
             int32_t acc[PAIR_COLS];
@@ -799,6 +827,62 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
                 store_tile_rows<kRawInt32, kAct, false, PAIR_COLS, 1>(
                     p, &tmY, out_smem, store_iter, mt * 2 * BMC + static_cast<int64_t>(rank) * BMC + q * 32,
                     nt * BNP + part * PAIR_COLS, acc, lane, ncols);
+            }
+        }
+        {  // the last, partial wave: its tiles split along N into items (the same steps)
+            const int sp = p.tail_split, wd = BNP / sp;
+            const int64_t n_items = (n_tiles - p.full_tiles) * sp;
+            const int rest = wd - part * PAIR_COLS;
+            const int ncols = rest < PAIR_COLS ? (rest > 0 ? rest : 0) : PAIR_COLS;
+            for (int64_t u = pair_id; u < n_items && ok; u += n_pairs) {  // (16-column drains: fewer live registers)
+                int64_t mt, nt;
+                tile_coords(p.full_tiles + u / sp, n_mt, n_nt, mt, nt);
+                const int coff = static_cast<int>(u % sp) * wd;
+                int32_t acc[PAIR_COLS];
+#pragma unroll
+                for (int i = 0; i < PAIR_COLS; ++i) acc[i] = 0;
+                for (int c = 0; c < n_chunks; ++c, ++chunk_iter) {
+                    const uint32_t buf = chunk_iter & 1u;
+                    if (*abort_flag || !mbar_wait(accf_bar(buf), (chunk_iter >> 1) & 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t taddr = tmem_base + lane_off + buf * BNP + part * PAIR_COLS;
+#pragma unroll
+                    for (int j = 0; j < PAIR_COLS / 16; ++j) {
+                        if (j * 16 >= ncols) break;  // an item narrower than this slice
+                        uint32_t r[16];
+                        tmem_ld16(taddr + j * 16, r);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) acc[j * 16 + i] += __float2int_rn(__uint_as_float(r[i]));
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) arrive_remote(map_to_rank(acce_bar(buf), 0));
+                }
+                if (!ok) break;
+                if constexpr (kLora) {
+                    const uint32_t buf = chunk_iter & 1u;
+                    if (*abort_flag || !mbar_wait(accf_bar(buf), (chunk_iter >> 1) & 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    // the LoRA chunk stays in tensor memory until the store reads it box by box
+                    store_tile_rows<kRawInt32, kAct, true, PAIR_COLS, 1>(
+                        p, &tmY, out_smem, store_iter, mt * 2 * BMC + static_cast<int64_t>(rank) * BMC + q * 32,
+                        nt * BNP + coff + part * PAIR_COLS, acc, lane, ncols,
+                        tmem_base + lane_off + buf * BNP + part * PAIR_COLS);
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) arrive_remote(map_to_rank(acce_bar(buf), 0));
+                    ++chunk_iter;
+                } else {
+                    store_tile_rows<kRawInt32, kAct, false, PAIR_COLS, 1>(
+                        p, &tmY, out_smem, store_iter, mt * 2 * BMC + static_cast<int64_t>(rank) * BMC + q * 32,
+                        nt * BNP + coff + part * PAIR_COLS, acc, lane, ncols);
+                }
             }
         }
         drain_stores(lane);
@@ -863,10 +947,22 @@ cudaError_t launch_pair(const GemmArgs &g, TcParams p, const CUtensorMap &ty, in
     const int64_t tiles = ((g.m + 2 * pair::BMC - 1) / (2 * pair::BMC)) * ((g.n + BN - 1) / BN);
     const int64_t pairs = tiles < sms / 2 ? tiles : sms / 2;
     const unsigned grid = static_cast<unsigned>(2 * pairs);
+    // The last, partial wave: when all of its tiles fit split along N (into up
+    // to eight items of 32 columns or more), the items spread over that many
+    // more pairs. (Not with a LoRA chunk, whose operands keep whole-tile boxes.)
+    const int64_t full = tiles / pairs * pairs, tail = tiles - full;
+    int split = 1;
+    if (g.lora_r == 0 && BN == 256 && tail > 0)
+        while (split < 8 && tail * split * 2 <= pairs) split *= 2;
+    p.full_tiles = full;
+    p.tail_split = split;
+    CUtensorMap pbt = pb;
+    if (split > 1 && !make_map(&pbt, g.qw, g.n, g.kpad, g.ldqw, static_cast<uint32_t>(C::BNC / split)))
+        return cudaErrorInvalidValue;
     auto run = [&](auto kern) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
         if (e != cudaSuccess) return e;
-        kern<<<grid, pair::PAIR_THREADS, C::SMEM_BYTES, stream>>>(pa, pb, ty, la, lb, p);
+        kern<<<grid, pair::PAIR_THREADS, C::SMEM_BYTES, stream>>>(pa, pb, ty, la, lb, pbt, p);
         return cudaGetLastError();
     };
     if (g.a) return run(pair::gemm_tc_pair_kernel<BN, true, 0, false>);

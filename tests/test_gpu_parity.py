@@ -253,6 +253,38 @@ def test_gemm_identical_codes_bit_exact(m, n, k, G, codes):
     parity.check_y_same_codes(Y0.cpu().numpy(), Y64n, A_ref, sx, sw, None)
 
 
+@pytest.mark.parametrize("m,n,act", [(512, 10240, 0), (512, 13468, 2), (300, 10112, 1), (512, 9984, 0),
+                                     (768, 9984, 0)])
+def test_gemm_split_last_wave_bit_exact(m, n, act):
+    """Shapes whose last, partial wave of 256 x 256 tiles is split along N
+    into items, on a 152-SM GB300: 80 tiles (4 past 76 pairs: 32-wide items),
+    106 tiles (30 past: 128-wide items, the ragged last column of tiles among
+    them), 80 tiles with ragged M, 78 tiles (2 past: 32-wide items), and 117
+    tiles (41 past: too many to split, so whole tiles through the same last-
+    wave loop). A is bit-exact and Y (with and without GELU) matches the
+    oracle, canaries intact."""
+    k = 320
+    rng = np.random.default_rng(m + n + act)
+    Qx, Qw = random_codes(rng, m, k), random_codes(rng, n, k)
+    sx = rng.uniform(0.001, 1.0, m).astype(np.float32)
+    sw = rng.uniform(0.0001, 0.01, n).astype(np.float32)
+    b = rng.standard_normal(n).astype(np.float32)
+    px = cr.packed_from_codes(to_dev(Qx), to_dev(sx), 64, cr.CODES_BF16)
+    pw = cr.packed_from_codes(to_dev(Qw), to_dev(sw), 64, cr.CODES_BF16)
+    Abig = torch.full((m + 1, (n + 7) // 4 * 4), -5, dtype=torch.int32, device="cuda")
+    A = cr.convrot_gemm_i32(px, pw, out=Abig[:m, :n])
+    Ybig = torch.full((m + 1, (n + 7) // 4 * 4), -3.0, dtype=torch.float32, device="cuda")
+    Y = cr.convrot_linear_act(px, pw, to_dev(b), act, out=Ybig[:m, :n])
+    torch.cuda.synchronize()
+    A_ref = oracle.gemm_i32(Qx, Qw, k)
+    np.testing.assert_array_equal(A.cpu().numpy(), A_ref)
+    assert torch.all(Abig[m:] == -5) and torch.all(Abig[:, n:] == -5)
+    assert torch.all(Ybig[m:] == -3.0) and torch.all(Ybig[:, n:] == -3.0)
+    _, Y64 = oracle.reconstruct(A_ref, sx, sw, b, act)
+    check = parity.check_y_act_same_codes if act else parity.check_y_same_codes
+    check(Y.cpu().numpy(), Y64, A_ref, sx, sw, b)
+
+
 @pytest.mark.parametrize("codes", GEMM_CODES, ids=GEMM_IDS)
 def test_gemm_saturated_int32_headroom(codes):
     """All-+-127 codes at k = 12288: |A| reaches 16129 * k = 198,193,152."""
@@ -310,8 +342,10 @@ def test_full_size_sampled(name):
     X, W, b = inputs.activations(wl), inputs.weights(wl), inputs.bias(wl)
     px = cr.convrot_pack_activations(to_dev(X), wl.G, codes)
     pw = cr.convrot_quantize_weights(to_dev(W), wl.G, codes)
-    Y = cr.convrot_linear(px, pw, to_dev(b))
+    # NaN-filled output: a tile the GEMM skipped cannot pass for a stale correct one
+    Y = cr.convrot_linear(px, pw, to_dev(b), out=torch.full((wl.m, wl.n), float("nan"), device="cuda"))
     torch.cuda.synchronize()
+    assert not torch.isnan(Y).any()
     rng = np.random.default_rng(123)
     n_rows = 96 if wl.m * wl.n * wl.k > 2e12 else 128
     rows = np.unique(np.concatenate([rng.choice(wl.m - 8, n_rows, replace=False),
@@ -372,8 +406,10 @@ def test_full_size_attention_grouped_qkv():
     bs = [inputs.bias(wl, i) for i in range(3)]
     px = cr.convrot_pack_activations(to_dev(X), wl.G, cr.CODES_BF16)
     pw = cr.quantize_weights_grouped([to_dev(W) for W in Ws], wl.G, cr.CODES_BF16)
-    Y = cr.convrot_linear(px, pw, to_dev(np.concatenate(bs)))
+    Y = cr.convrot_linear(px, pw, to_dev(np.concatenate(bs)),
+                          out=torch.full((wl.m, 3 * wl.n), float("nan"), device="cuda"))
     torch.cuda.synchronize()
+    assert not torch.isnan(Y).any()
     rows = np.concatenate([np.random.default_rng(5).choice(wl.m - 8, 48, replace=False), np.arange(wl.m - 8, wl.m)])
     Qx_ref, sx_ref, vx = oracle.pack_rows(X[rows], wl.G)
     Qw_ref, sw_ref, _ = oracle.pack_rows(np.concatenate(Ws), wl.G, want_pre_round=False)
