@@ -589,7 +589,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
     gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmLa,
                         const __grid_constant__ CUtensorMap tmLb, const __grid_constant__ CUtensorMap tmBt,
-                        TcParams p)
+                        const __grid_constant__ CUtensorMap tmLbt, TcParams p)
 {
     using C = Cfg<BN>;
     constexpr int STAGES = C::STAGES, STAGE_BYTES = C::STAGE_BYTES, A_BYTES = C::A_BYTES, BNP = C::BNP, BNC = C::BNC;
@@ -664,7 +664,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
             int issued = 0;
             bool ok = true;
             // one tile or item: every K slice of its A rows and of this CTA's brow.. B rows
-            auto produce = [&](int mt, int brow, uint32_t tx, const CUtensorMap *bmap) {
+            auto produce = [&](int mt, int brow, uint32_t tx, const CUtensorMap *bmap, const CUtensorMap *lbmap) {
                 const int arow = mt * 2 * BMC + static_cast<int>(rank) * BMC;
                 for (int ks = 0; ks < kst + lkst; ++ks) {
                     if (*abort_flag || !mbar_wait(empty_bar(stage), phase ^ 1u)) {
@@ -677,7 +677,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
                     const bool lo = kLora && ks >= kst;
                     const int kx = (lo ? ks - kst : ks) * BK;
                     tma_load_2d_pair(sa, lo ? &tmLa : &tmA, kx, arow, lbar);
-                    tma_load_2d_pair(sa + A_BYTES, lo ? &tmLb : bmap, kx, brow, lbar);
+                    tma_load_2d_pair(sa + A_BYTES, lo ? lbmap : bmap, kx, brow, lbar);
                     ++issued;
                     if (++stage == STAGES) {
                         stage = 0;
@@ -689,7 +689,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
                 int64_t mt64, nt64;
                 tile_coords(t, n_mt, n_nt, mt64, nt64);
                 produce(static_cast<int>(mt64), static_cast<int>(nt64) * BNP + static_cast<int>(rank) * BNC,
-                        2u * STAGE_BYTES, &tmB);
+                        2u * STAGE_BYTES, &tmB, &tmLb);
             }
             {  // the last, partial wave: its tiles split along N into items
                 const int sp = p.tail_split, wd = BNP / sp;
@@ -700,7 +700,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
                     const int brow = static_cast<int>(nt64) * BNP + static_cast<int>(u % sp) * wd +
                                      static_cast<int>(rank) * (wd / 2);
                     produce(static_cast<int>(mt64), brow, 2u * static_cast<uint32_t>(A_BYTES + (wd / 2) * BK * 2),
-                            sp > 1 ? &tmBt : &tmB);
+                            sp > 1 ? &tmBt : &tmB, sp > 1 ? &tmLbt : &tmLb);
                 }
             }
             if (!ok) {
@@ -949,20 +949,24 @@ cudaError_t launch_pair(const GemmArgs &g, TcParams p, const CUtensorMap &ty, in
     const unsigned grid = static_cast<unsigned>(2 * pairs);
     // The last, partial wave: when all of its tiles fit split along N (into up
     // to eight items of 32 columns or more), the items spread over that many
-    // more pairs. (Not with a LoRA chunk, whose operands keep whole-tile boxes.)
+    // more pairs. B (and the LoRA chunk's B_ext) then come in narrower boxes.
     const int64_t full = tiles / pairs * pairs, tail = tiles - full;
     int split = 1;
-    if (g.lora_r == 0 && BN == 256 && tail > 0)
+    if (BN == 256 && tail > 0)
         while (split < 8 && tail * split * 2 <= pairs) split *= 2;
     p.full_tiles = full;
     p.tail_split = split;
-    CUtensorMap pbt = pb;
-    if (split > 1 && !make_map(&pbt, g.qw, g.n, g.kpad, g.ldqw, static_cast<uint32_t>(C::BNC / split)))
-        return cudaErrorInvalidValue;
+    CUtensorMap pbt = pb, lbt = lb;
+    if (split > 1) {
+        const uint32_t rows = static_cast<uint32_t>(C::BNC / split);
+        if (!make_map(&pbt, g.qw, g.n, g.kpad, g.ldqw, rows)) return cudaErrorInvalidValue;
+        if (g.lora_r > 0 && !make_map(&lbt, g.lora_b, g.n, lora_cols(g.lora_r), g.lora_ldb, rows))
+            return cudaErrorInvalidValue;
+    }
     auto run = [&](auto kern) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
         if (e != cudaSuccess) return e;
-        kern<<<grid, pair::PAIR_THREADS, C::SMEM_BYTES, stream>>>(pa, pb, ty, la, lb, pbt, p);
+        kern<<<grid, pair::PAIR_THREADS, C::SMEM_BYTES, stream>>>(pa, pb, ty, la, lb, pbt, lbt, p);
         return cudaGetLastError();
     };
     if (g.a) return run(pair::gemm_tc_pair_kernel<BN, true, 0, false>);

@@ -493,10 +493,12 @@ def test_lora_down_against_oracle(m, k, r):
 
 
 @pytest.mark.parametrize("m,n,k,r,act", [(300, 300, 512, 32, 0), (300, 512, 1024, 64, 1), (64, 1000, 256, 16, 2),
-                                         (513, 256, 3072, 128, 0)])
+                                         (513, 256, 3072, 128, 0), (512, 10240, 320, 64, 0),
+                                         (512, 13468, 320, 32, 2)])
 def test_linear_lora_identical_codes(m, n, k, r, act):
     """Y = act(A s_x s_w + b + scale (X A_l^T) B_l^T) with the LoRA term as an extra
-    fp32 chunk of the pair GEMM (also for m <= 128)."""
+    fp32 chunk of the pair GEMM (also for m <= 128, and for shapes whose last,
+    partial wave is split along N into 32- and 128-wide items on a 152-SM GB300)."""
     rng = np.random.default_rng(m * 3 + n + k + r)
     X = special_rows(rng, m, k)
     Qx, Qw = random_codes(rng, m, k), random_codes(rng, n, k)
