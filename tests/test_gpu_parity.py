@@ -336,7 +336,8 @@ FULL = ["attn_qkv", "mlp_up", "mlp_down", "sweep_G4", "sweep_G16", "sweep_G64", 
 @pytest.mark.slow
 @pytest.mark.parametrize("name", FULL)
 def test_full_size_sampled(name):
-    """Full workload on the GPU in the bench's configuration; oracle on sampled rows."""
+    """Full workload on the GPU in the bench's configuration: the pack against the
+    oracle on every row, Y on sampled rows plus the tail."""
     wl = inputs.WORKLOADS[name]
     codes = GEMM_CODES[-1]
     X, W, b = inputs.activations(wl), inputs.weights(wl), inputs.bias(wl)
@@ -346,8 +347,18 @@ def test_full_size_sampled(name):
     Y = cr.convrot_linear(px, pw, to_dev(b), out=torch.full((wl.m, wl.n), float("nan"), device="cuda"))
     torch.cuda.synchronize()
     assert not torch.isnan(Y).any()
+    # the pack on every row, in chunks of rows: scales and codes against the oracle
+    sx_all, qx_all = px.scale.cpu().numpy(), codes_np(px)
+    for r0 in range(0, wl.m, 4096):
+        r1 = min(wl.m, r0 + 4096)
+        Qc, sc, vc = oracle.pack_rows(X[r0:r1], wl.G)
+        parity.check_scales(sx_all[r0:r1], sc)
+        parity.check_codes(qx_all[r0:r1], Qc, vc)
+        del Qc, sc, vc
+    del qx_all
+    # Y on 512 seeded random rows (256 on the largest shape) plus the tail rows
     rng = np.random.default_rng(123)
-    n_rows = 96 if wl.m * wl.n * wl.k > 2e12 else 128
+    n_rows = 256 if wl.m * wl.n * wl.k > 2e12 else 512
     rows = np.unique(np.concatenate([rng.choice(wl.m - 8, n_rows, replace=False),
                                      np.arange(wl.m - 8, wl.m)]))
     Xs = X[rows]
