@@ -133,12 +133,23 @@ struct TcParams {
 // loop unrolled only twice so that the accumulators of the boxes still to
 // come stay in registers while it runs (fully unrolled, the GELU's
 // temporaries pushed all 128 of them to local memory).
-template <int kAct>
+// Staged box of 32 rows x BW fp32 columns (BW = 32: 128-byte rows in the
+// 128-byte swizzle, 16-byte chunk c of row r at c ^ (r & 7); BW = 16: 64-byte
+// rows in the 64-byte swizzle, chunk c at c ^ ((r >> 1) & 3)); either way the
+// row-per-lane 16-byte writes are conflict-free.
+template <int BW>
+__device__ __forceinline__ uint32_t box_addr(uint32_t buf, int lane, int c)
+{
+    const int phys = BW == 32 ? (c ^ (lane & 7)) : (c ^ ((lane >> 1) & 3));
+    return buf + lane * (BW * 4) + (phys << 4);
+}
+
+template <int kAct, int BW = 32>
 __device__ __forceinline__ void act_box(uint32_t buf, int lane)
 {
 #pragma unroll 2
-    for (int c = 0; c < 8; ++c) {
-        const uint32_t addr = buf + lane * (OUT_BOX * 4) + ((c ^ (lane & 7)) << 4);
+    for (int c = 0; c < BW / 4; ++c) {
+        const uint32_t addr = box_addr<BW>(buf, lane, c);
         float4 v;
         asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
         v = make_float4(apply_act_t<kAct>(v.x), apply_act_t<kAct>(v.y), apply_act_t<kAct>(v.z), apply_act_t<kAct>(v.w));
@@ -149,8 +160,9 @@ __device__ __forceinline__ void act_box(uint32_t buf, int lane)
 
 // With kLora, lora_taddr is the TMEM address of this warp's rows and columns
 // of the LoRA chunk (fp32), added to each output before the activation.
-// NACC: columns per warp (128 or 64); NBUF: the warp's staging buffers (2 or 1).
-template <bool kRawInt32, int kAct, bool kLora = false, int NACC = 128, int NBUF = 2>
+// NACC: columns per warp (128 or 64); NBUF: the warp's staging buffers (2 or 1);
+// BW: columns per staged box (32 or 16).
+template <bool kRawInt32, int kAct, bool kLora = false, int NACC = 128, int NBUF = 2, int BW = 32>
 __device__ __forceinline__ void store_tile_rows(const TcParams &p, const CUtensorMap *tmY, uint32_t out_smem,
                                                 uint32_t &store_iter, int64_t row0, int64_t col0,
                                                 const int32_t (&acc)[NACC], int lane, int ncols = NACC,
@@ -159,39 +171,40 @@ __device__ __forceinline__ void store_tile_rows(const TcParams &p, const CUtenso
     const int64_t row = row0 + lane;
     float sxr = 0.0f;
     if constexpr (!kRawInt32) sxr = row < p.m ? p.sx[row] : 0.0f;
+    constexpr uint32_t kBufBytes = 32u * BW * 4u;
 #pragma unroll
-    for (int cc = 0; cc < NACC / 32; ++cc) {
-        if (cc * 32 >= ncols) break;
-        const int64_t x = col0 + cc * 32;
+    for (int cc = 0; cc < NACC / BW; ++cc) {
+        if (cc * BW >= ncols) break;
+        const int64_t x = col0 + cc * BW;
         if (x >= p.n) break;
-        if ((kAct != 0 || kLora) && x + 32 > p.n) {
+        if ((kAct != 0 || kLora) && x + BW > p.n) {
             // ragged last box with an activation or a LoRA term: stage, activate, then masked stores
-            const uint32_t buf = out_smem + (NBUF == 2 ? (store_iter & 1u) * OUT_BUF_BYTES : 0u);
+            const uint32_t buf = out_smem + (NBUF == 2 ? (store_iter & 1u) * kBufBytes : 0u);
             if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
             __syncwarp();
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
+            for (int c = 0; c < BW / 4; ++c) {
                 uint32_t w[4], lr[4];
-                if constexpr (kLora) tmem_ld4(lora_taddr + cc * 32 + c * 4, lr);
+                if constexpr (kLora) tmem_ld4(lora_taddr + cc * BW + c * 4, lr);
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int64_t col = x + c * 4 + e;
                     const float swv = col < p.n ? __ldg(p.sw + col) : 0.0f;
                     const float bv = (p.bias && col < p.n) ? __ldg(p.bias + col) : 0.0f;
-                    float y = fmaf(static_cast<float>(acc[cc * 32 + c * 4 + e]) * sxr, swv, bv);
+                    float y = fmaf(static_cast<float>(acc[cc * BW + c * 4 + e]) * sxr, swv, bv);
                     if constexpr (kLora) y += __uint_as_float(lr[e]);
                     w[e] = __float_as_uint(y);
                 }
-                const uint32_t addr = buf + lane * (OUT_BOX * 4) + ((c ^ (lane & 7)) << 4);
+                const uint32_t addr = box_addr<BW>(buf, lane, c);
                 asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[0]), "r"(w[1]), "r"(w[2]),
                              "r"(w[3])
                              : "memory");
             }
-            if constexpr (kAct != 0) act_box<kAct>(buf, lane);
+            if constexpr (kAct != 0) act_box<kAct, BW>(buf, lane);
             if (row < p.m) {
 #pragma unroll 1
-                for (int j = 0; j < 32 && x + j < p.n; ++j) {
-                    const uint32_t addr = buf + lane * (OUT_BOX * 4) + ((((j >> 2) ^ (lane & 7)) << 4) | ((j & 3) << 2));
+                for (int j = 0; j < BW && x + j < p.n; ++j) {
+                    const uint32_t addr = box_addr<BW>(buf, lane, j >> 2) | ((j & 3) << 2);
                     float v;
                     asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
                     p.y[row * p.ldy + x + j] = v;
@@ -200,22 +213,22 @@ __device__ __forceinline__ void store_tile_rows(const TcParams &p, const CUtenso
             __syncwarp();
             continue;
         }
-        if (x + 32 > p.n) {
+        if (x + BW > p.n) {
             // ragged last box: masked stores straight from registers
             if (row < p.m) {
-                for (int j = 0; j < 32 && x + j < p.n; ++j) {
+                for (int j = 0; j < BW && x + j < p.n; ++j) {
                     const int64_t col = x + j;
                     if constexpr (kRawInt32) {
-                        p.a[row * p.ldy + col] = acc[cc * 32 + j];
+                        p.a[row * p.ldy + col] = acc[cc * BW + j];
                     } else {
                         const float b = p.bias ? __ldg(p.bias + col) : 0.0f;
-                        p.y[row * p.ldy + col] = fmaf(static_cast<float>(acc[cc * 32 + j]) * sxr, __ldg(p.sw + col), b);
+                        p.y[row * p.ldy + col] = fmaf(static_cast<float>(acc[cc * BW + j]) * sxr, __ldg(p.sw + col), b);
                     }
                 }
             }
             continue;
         }
-        const uint32_t buf = out_smem + (NBUF == 2 ? (store_iter & 1u) * OUT_BUF_BYTES : 0u);
+        const uint32_t buf = out_smem + (NBUF == 2 ? (store_iter & 1u) * kBufBytes : 0u);
         if (lane == 0) {
             if constexpr (NBUF == 2)
                 asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
@@ -224,9 +237,9 @@ __device__ __forceinline__ void store_tile_rows(const TcParams &p, const CUtenso
         }
         __syncwarp();
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
+        for (int c = 0; c < BW / 4; ++c) {
             uint32_t w[4], lr[4];
-            if constexpr (kLora) tmem_ld4(lora_taddr + cc * 32 + c * 4, lr);
+            if constexpr (kLora) tmem_ld4(lora_taddr + cc * BW + c * 4, lr);
             float4 sw4 = make_float4(0.f, 0.f, 0.f, 0.f), b4 = make_float4(0.f, 0.f, 0.f, 0.f);
             if constexpr (!kRawInt32) {
                 const int64_t col = x + c * 4;
@@ -243,7 +256,7 @@ __device__ __forceinline__ void store_tile_rows(const TcParams &p, const CUtenso
             const float swv[4] = {sw4.x, sw4.y, sw4.z, sw4.w}, bv[4] = {b4.x, b4.y, b4.z, b4.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const int j = cc * 32 + c * 4 + e;
+                const int j = cc * BW + c * 4 + e;
                 if constexpr (kRawInt32) {
                     w[e] = static_cast<uint32_t>(acc[j]);
                 } else {
@@ -253,7 +266,7 @@ __device__ __forceinline__ void store_tile_rows(const TcParams &p, const CUtenso
                     w[e] = __float_as_uint(y);
                 }
             }
-            const uint32_t addr = buf + lane * (OUT_BOX * 4) + ((c ^ (lane & 7)) << 4);
+            const uint32_t addr = box_addr<BW>(buf, lane, c);
             asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[0]), "r"(w[1]), "r"(w[2]),
                          "r"(w[3])
                          : "memory");
@@ -485,6 +498,12 @@ namespace pair {
 
 constexpr int BMC = 128;  // rows of A and D per CTA (256 per pair)
 
+// Y staging of the pair kernel's sixteen epilogue warps: PAIR_NBUF buffers of
+// one 32 x PAIR_BW fp32 box each per warp.
+constexpr int PAIR_BW = 16, PAIR_NBUF = 1;
+constexpr int PAIR_BUF_BYTES = 32 * PAIR_BW * 4;
+constexpr int PAIR_OUT_BYTES = 16 * PAIR_NBUF * PAIR_BUF_BYTES;
+
 // Tile width of a pair: BN columns of D (BN / 2 rows of B in each CTA).
 template <int BN>
 struct Cfg {
@@ -494,10 +513,10 @@ struct Cfg {
     static constexpr int A_BYTES = BMC * BK * 2;
     static constexpr int B_BYTES = BNC * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int STAGES = (232448 - 1024 - OUT_BYTES - BAR_BYTES) / STAGE_BYTES < 6
-                                      ? (232448 - 1024 - OUT_BYTES - BAR_BYTES) / STAGE_BYTES
+    static constexpr int STAGES = (232448 - 1024 - PAIR_OUT_BYTES - BAR_BYTES) / STAGE_BYTES < 6
+                                      ? (232448 - 1024 - PAIR_OUT_BYTES - BAR_BYTES) / STAGE_BYTES
                                       : 6;
-    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + OUT_BYTES + BAR_BYTES;
+    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + PAIR_OUT_BYTES + BAR_BYTES;
     // kind::f16: D fp32, A and B bf16, K-major, M = 256 (both CTAs), N = BN
     static constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(BN >> 3) << 17) |
                                        (uint32_t(256 >> 4) << 24);
@@ -579,7 +598,7 @@ constexpr int PAIR_THREADS = 128 + PAIR_EPI_WARPS * 32;
 constexpr int PAIR_COLS = 64;  // columns per epilogue warp
 constexpr int kRegsWg0 = 40, kRegsEpi = 104;
 static_assert(4 * 32 * kRegsWg0 + PAIR_EPI_WARPS * 32 * kRegsEpi <= PAIR_THREADS * 96, "register split");
-static_assert(PAIR_EPI_WARPS * OUT_BUF_BYTES <= OUT_BYTES, "one staging box per epilogue warp");
+static_assert(PAIR_EPI_WARPS * PAIR_NBUF * PAIR_BUF_BYTES == PAIR_OUT_BYTES, "staging per epilogue warp");
 
 // kLora: after each tile's K slices, the producer streams lora_kst more slices
 // from tmLa (T_ext rows) and tmLb (B_ext rows); the MMA runs them as one extra
@@ -598,14 +617,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *gbase = smem_raw + (base - raw);
     const uint32_t out_base = base + STAGES * STAGE_BYTES;
-    const uint32_t bars = out_base + OUT_BYTES;
+    const uint32_t bars = out_base + PAIR_OUT_BYTES;
     auto full_bar = [&](int s) { return bars + 8u * s; };
     auto empty_bar = [&](int s) { return bars + 8u * (STAGES + s); };
     auto accf_bar = [&](int b) { return bars + 8u * (2 * STAGES + b); };
     auto acce_bar = [&](int b) { return bars + 8u * (2 * STAGES + 2 + b); };
     const uint32_t done_bar = bars + 8u * (2 * STAGES + 4);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + STAGES * STAGE_BYTES + OUT_BYTES + 160);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + STAGES * STAGE_BYTES + OUT_BYTES + 164);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + STAGES * STAGE_BYTES + PAIR_OUT_BYTES + 160);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + STAGES * STAGE_BYTES + PAIR_OUT_BYTES + 164);
 
     const uint32_t rank = cluster_rank();
     const bool leader = rank == 0;
@@ -775,7 +794,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
         const int q = warp & 3;            // TMEM lane quadrant (warp % 4)
         const int part = (warp - 4) >> 2;  // 64-column slice of the tile or item
         const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
-        const uint32_t out_smem = out_base + (warp - 4) * OUT_BUF_BYTES;
+        const uint32_t out_smem = out_base + (warp - 4) * PAIR_NBUF * PAIR_BUF_BYTES;
         uint32_t store_iter = 0;
         uint32_t chunk_iter = 0;
         bool ok = true;
@@ -816,7 +835,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
                 }
                 tc_fence_after();
                 // the LoRA chunk stays in tensor memory until the store reads it box by box
-                store_tile_rows<kRawInt32, kAct, true, PAIR_COLS, 1>(
+                store_tile_rows<kRawInt32, kAct, true, PAIR_COLS, PAIR_NBUF, PAIR_BW>(
                     p, &tmY, out_smem, store_iter, mt * 2 * BMC + static_cast<int64_t>(rank) * BMC + q * 32,
                     nt * BNP + part * PAIR_COLS, acc, lane, ncols, tmem_base + lane_off + buf * BNP + part * PAIR_COLS);
                 tc_fence_before();
@@ -824,7 +843,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
                 if (lane == 0) arrive_remote(map_to_rank(acce_bar(buf), 0));
                 ++chunk_iter;
             } else {
-                store_tile_rows<kRawInt32, kAct, false, PAIR_COLS, 1>(
+                store_tile_rows<kRawInt32, kAct, false, PAIR_COLS, PAIR_NBUF, PAIR_BW>(
                     p, &tmY, out_smem, store_iter, mt * 2 * BMC + static_cast<int64_t>(rank) * BMC + q * 32,
                     nt * BNP + part * PAIR_COLS, acc, lane, ncols);
             }
@@ -870,7 +889,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
                     }
                     tc_fence_after();
                     // the LoRA chunk stays in tensor memory until the store reads it box by box
-                    store_tile_rows<kRawInt32, kAct, true, PAIR_COLS, 1>(
+                    store_tile_rows<kRawInt32, kAct, true, PAIR_COLS, PAIR_NBUF, PAIR_BW>(
                         p, &tmY, out_smem, store_iter, mt * 2 * BMC + static_cast<int64_t>(rank) * BMC + q * 32,
                         nt * BNP + coff + part * PAIR_COLS, acc, lane, ncols,
                         tmem_base + lane_off + buf * BNP + part * PAIR_COLS);
@@ -879,7 +898,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
                     if (lane == 0) arrive_remote(map_to_rank(acce_bar(buf), 0));
                     ++chunk_iter;
                 } else {
-                    store_tile_rows<kRawInt32, kAct, false, PAIR_COLS, 1>(
+                    store_tile_rows<kRawInt32, kAct, false, PAIR_COLS, PAIR_NBUF, PAIR_BW>(
                         p, &tmY, out_smem, store_iter, mt * 2 * BMC + static_cast<int64_t>(rank) * BMC + q * 32,
                         nt * BNP + coff + part * PAIR_COLS, acc, lane, ncols);
                 }
@@ -914,25 +933,30 @@ bool make_map(CUtensorMap *map, const void *base, int64_t rows, int64_t kpad, in
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 2-D map over the [m, ld] output (fp32 Y or int32 A), 32 x 32 boxes, 128-byte swizzle.
-bool make_out_map(CUtensorMap *map, void *base, int64_t m, int64_t n, int64_t ld, bool int32_out)
+// 2-D map over the [m, ld] output (fp32 Y or int32 A): 32 rows x box_cols boxes,
+// 128-byte swizzle for 32 columns, 64-byte swizzle for 16.
+bool make_out_map(CUtensorMap *map, void *base, int64_t m, int64_t n, int64_t ld, bool int32_out, int box_cols = OUT_BOX)
 {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(m)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 4};
-    cuuint32_t box[2] = {static_cast<cuuint32_t>(OUT_BOX), static_cast<cuuint32_t>(OUT_BOX)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(OUT_BOX)};
     cuuint32_t estr[2] = {1, 1};
     return fn(map, int32_out ? CU_TENSOR_MAP_DATA_TYPE_INT32 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides,
-              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              box_cols == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int BN>
-cudaError_t launch_pair(const GemmArgs &g, TcParams p, const CUtensorMap &ty, int sms, cudaStream_t stream)
+cudaError_t launch_pair(const GemmArgs &g, TcParams p, int sms, cudaStream_t stream)
 {
     using C = pair::Cfg<BN>;
-    CUtensorMap pa, pb, la, lb;
+    CUtensorMap pa, pb, la, lb, ty;
+    if (!make_out_map(&ty, g.a ? static_cast<void *>(g.a) : static_cast<void *>(g.y), g.m, g.n, g.ldy, g.a != nullptr,
+                      pair::PAIR_BW))
+        return cudaErrorInvalidValue;
     if (!make_map(&pa, g.qx, g.m, g.kpad, g.ldqx, pair::BMC) || !make_map(&pb, g.qw, g.n, g.kpad, g.ldqw, C::BNC))
         return cudaErrorInvalidValue;
     la = pa;
@@ -1010,7 +1034,7 @@ cudaError_t launch_gemm_tc(const GemmArgs &g, cudaStream_t stream)
         // CTA pairs on 256 x 256 tiles. (224-wide tiles fill the last wave better on
         // paper but measured no faster on the DiT shapes: each chunk already runs at
         // close to the tensor peak and per-tile costs do not shrink with the width.)
-        return launch_pair<256>(g, p, ty, sms, stream);
+        return launch_pair<256>(g, p, sms, stream);
     }
     const int64_t tiles = ((g.m + BM - 1) / BM) * ((g.n + BN - 1) / BN);
     const unsigned grid = static_cast<unsigned>(tiles < sms ? tiles : sms);
