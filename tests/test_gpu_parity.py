@@ -286,17 +286,20 @@ def test_gemm_split_last_wave_bit_exact(m, n, act):
 
 
 @pytest.mark.parametrize("codes", GEMM_CODES, ids=GEMM_IDS)
-def test_gemm_saturated_int32_headroom(codes):
-    """All-+-127 codes at k = 12288: |A| reaches 16129 * k = 198,193,152."""
+@pytest.mark.parametrize("k,G", [(12288, 256), (133144, 4)])
+def test_gemm_saturated_int32_headroom(codes, k, G):
+    """All-+-127 codes: |A| reaches 16129 * k, 198,193,152 at k = 12288 and, at the
+    largest k the ABI accepts (133144, 131 exact fp32 chunks on the tensor-core
+    path), 2,147,479,576: 4,071 below the int32 limit."""
     rng = np.random.default_rng(1)
-    m, n, k = 130, 136, 12288
+    m, n = 130, 136
     Qx = random_codes(rng, m, k, sat=True)
     Qw = random_codes(rng, n, k, sat=True)
     Qx[0] = 127
     Qw[0] = 127
     Qw[1] = -127
-    px = cr.packed_from_codes(to_dev(Qx), torch.ones(m, device="cuda"), 256, codes)
-    pw = cr.packed_from_codes(to_dev(Qw), torch.ones(n, device="cuda"), 256, codes)
+    px = cr.packed_from_codes(to_dev(Qx), torch.ones(m, device="cuda"), G, codes)
+    pw = cr.packed_from_codes(to_dev(Qw), torch.ones(n, device="cuda"), G, codes)
     A = cr.convrot_gemm_i32(px, pw).cpu().numpy()
     A_ref = oracle.gemm_i32(Qx, Qw, k)
     assert A_ref[0, 0] == 16129 * k and A_ref[0, 1] == -16129 * k
