@@ -235,20 +235,37 @@ convrot_status convrot_linear_lora(const convrot_packed *x, const convrot_packed
 
 /*
  * No counterpart on the page (an entry point of this library only): the LoRA
- * linear in one call that allocates nothing, not even T_ext. It runs
- * convrot_lora_down into a file-scope device array of the library
- * (CONVROT_NOALLOC_SCRATCH_BYTES, 256-byte aligned; its address comes from
- * cudaGetSymbolAddress on the current device), then convrot_linear_lora
- * reading it. Results equal those of the two calls with a caller's T_ext.
+ * linear in one call that allocates nothing, not even the T_ext that
+ * convrot_lora_down / convrot_linear_lora ask the caller for.
+ *
+ * Who needs it: callers that must not call cudaMalloc. A plug-in running
+ * inside a host application whose device memory belongs to that
+ * application's own pool (a framework's caching allocator, an arena sized
+ * once at start-up) cannot take memory behind the pool's back; a real-time
+ * or latency-bound loop cannot afford cudaMalloc's cost or the device-wide
+ * synchronization that an allocation or free may bring; and code with a
+ * fixed device-memory budget set at load time cannot grow it per call.
+ *
+ * It runs convrot_lora_down into a file-scope device array of the library
+ * (CONVROT_NOALLOC_SCRATCH_BYTES = 32 MiB, 256-byte aligned), then
+ * convrot_linear_lora reading it. Results equal those of the two calls with
+ * a caller's T_ext.
  *   X, ldx, A_ext, lda, k = x->k   as for convrot_lora_down.
  *   B_ext, lde, r, bias, act, Y, ldy, dev_status   as for convrot_linear_lora.
- * A request whose T_ext (x->rows * convrot_lora_cols(r) bf16) exceeds the
- * array returns CONVROT_ERR_SCRATCH and launches nothing; a failed address
- * lookup returns CONVROT_ERR_CUDA. Nothing in the array must start at zero
- * (the down kernel writes every column the GEMM reads, padding included).
- * The array is one per device and process: calls that overlap in time (on
- * different streams, or from different host threads) race on it; serialize
- * them, e.g. on one stream.
+ * Limits and errors: a request whose T_ext (x->rows * convrot_lora_cols(r)
+ * bf16 values; e.g. up to 87381 rows at r = 64, 21845 at r = 256) exceeds
+ * the array returns CONVROT_ERR_SCRATCH and launches nothing; a failed
+ * address lookup returns CONVROT_ERR_CUDA.
+ * Set-up: the first call on a device (with that device current) looks up the
+ * array's device address with cudaGetSymbolAddress and keeps it for that
+ * device's context; make that first call before any stream capture.
+ * Sharing: every GPU that loads the library holds the array until the
+ * process exits, and every call on a device shares that device's array,
+ * which keeps the last call's contents. Nothing in it must start at zero
+ * (the down kernel writes every column the GEMM reads, padding included), so
+ * nothing is cleared. Calls that overlap on the GPU (on different streams,
+ * or from different host threads) race on it; serialize them, e.g. on one
+ * stream.
  */
 #define CONVROT_NOALLOC_SCRATCH_BYTES (32ll << 20)
 convrot_status convrot_linear_lora_noalloc(const convrot_packed *x, const convrot_packed *w, const float *bias,

@@ -311,8 +311,13 @@ def convrot_linear_lora(x: Packed, w: Packed, bias: torch.Tensor | None, act: in
 def convrot_linear_lora_noalloc(x: Packed, w: Packed, bias: torch.Tensor | None, act: int, X: torch.Tensor,
                                 A_ext: torch.Tensor, b_ext: torch.Tensor, r: int, out: torch.Tensor | None = None,
                                 dev_status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """The LoRA linear in one call, T_ext in the library's static device scratch (nothing
-    allocated; calls that overlap in time race on that scratch)."""
+    """The LoRA linear in one call that allocates no device memory, for callers that must
+    not call cudaMalloc (device memory owned by a host application's pool, no room for an
+    allocation's cost in a latency-bound loop, a fixed memory budget). T_ext goes to the
+    library's 32 MiB per-device static array; larger requests raise ERR_SCRATCH. The first
+    call on a device looks up that array's address: make it before any stream capture.
+    Every call shares the array, so calls that overlap on the GPU race on it. ``out`` is
+    allocated here only when the caller passes none; the C entry point allocates nothing."""
     if out is None:
         out = _padded_out(x.rows, w.rows, torch.float32, x.q.device)
     if bias is not None and (bias.dtype != torch.float32 or not bias.is_cuda):

@@ -1,15 +1,76 @@
 // C-ABI entry points of libconvrot: host-side validation, then launches.
 // The operations are those of the page "INT8 Convrot Safetensors"
 // (stable-diffusion.cpp docs); see include/convrot.h for the contract.
+#include <cuda.h>
+
 #include <cstdint>
+#include <mutex>
 
 #include "../../include/convrot.h"
 #include "internal.h"
 
 namespace {
 
-// Scratch of convrot_linear_lora_noalloc: T_ext, one array per device.
+// Scratch of convrot_linear_lora_noalloc: T_ext, one array per device. Every
+// GPU that loads the library holds it until the process exits. In host code
+// the name is a host-side stand-in: kernels get the device address that
+// noalloc_scratch_address looks up.
 static __device__ __align__(256) uint8_t g_noalloc_scratch[CONVROT_NOALLOC_SCRATCH_BYTES];
+
+// Unique id of the calling thread's current context (driver entry points
+// fetched through the runtime, so the library needs no libcuda at link time).
+bool current_context_id(unsigned long long *id)
+{
+    using GetCurrentFn = CUresult (*)(CUcontext *);
+    using GetIdFn = CUresult (*)(CUcontext, unsigned long long *);
+    static GetCurrentFn get_current = nullptr;
+    static GetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<GetCurrentFn>(p);
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<GetIdFn>(p);
+    });
+    CUcontext ctx = nullptr;
+    return get_current && get_id && get_current(&ctx) == CUDA_SUCCESS && ctx && get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// Device address of g_noalloc_scratch on the current device, or nullptr if
+// the lookup fails. It is looked up once per device (with that device
+// current), on the first call there, and kept with the id of the context it
+// belongs to, so that a new context after a cudaDeviceReset looks it up again.
+void *noalloc_scratch_address()
+{
+    constexpr int kMaxDevices = 64;
+    struct Entry {
+        unsigned long long ctx_id;
+        void *addr;
+    };
+    static Entry cache[kMaxDevices] = {};
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+    unsigned long long id = 0;
+    bool have_id = current_context_id(&id);
+    const bool cacheable = dev >= 0 && dev < kMaxDevices;
+    if (have_id && cacheable) {
+        std::lock_guard<std::mutex> g(mu);
+        if (cache[dev].addr && cache[dev].ctx_id == id) return cache[dev].addr;
+    }
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return nullptr;
+    if (!have_id) have_id = current_context_id(&id);  // the lookup made the device's context current
+    if (have_id && cacheable) {
+        std::lock_guard<std::mutex> g(mu);
+        cache[dev] = Entry{id, p};
+    }
+    return p;
+}
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -266,8 +327,8 @@ convrot_status convrot_linear_lora_noalloc(const convrot_packed *x, const convro
     if (x->rows > CONVROT_NOALLOC_SCRATCH_BYTES / (cols * 2)) return CONVROT_ERR_SCRATCH;
     if (x->rows == 0 || w->rows == 0) return convrot_linear_lora(x, w, bias, act, nullptr, cols, B_ext, lde, r, Y, ldy,
                                                                  dev_status, stream);
-    void *scratch = nullptr;
-    if (cudaGetSymbolAddress(&scratch, g_noalloc_scratch) != cudaSuccess || !scratch) return CONVROT_ERR_CUDA;
+    void *scratch = noalloc_scratch_address();
+    if (!scratch) return CONVROT_ERR_CUDA;
     convrot_status st = convrot_lora_down(X, x->rows, x->k, ldx, A_ext, r, lda, scratch, cols, dev_status, stream);
     if (st != CONVROT_OK) return st;
     return convrot_linear_lora(x, w, bias, act, scratch, cols, B_ext, lde, r, Y, ldy, dev_status, stream);

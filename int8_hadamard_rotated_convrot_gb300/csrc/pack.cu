@@ -33,15 +33,21 @@
 // (butterflies by warp shuffle) and the rest from the slot (register
 // butterflies). The float4 component is digit 0 of the in-group index.
 //
-// Launch shape. One kernel, loading registers straight from global memory
-// with streaming 16-byte loads: a CTA of about 128 threads owns whole rows
-// (96 threads per row at K = 3072), and many CTAs per SM overlap their
-// load / compute / store phases. Rows longer than 512 threads hold are split
-// over a thread-block cluster, whose CTAs exchange their partial row maxima
-// through distributed shared memory. (Persistent variants that stream rows
-// through a shared-memory ring with bulk copies, with or without a
-// shared-memory transpose in place of the lane shuffles, measured no faster
-// on any of the DiT shapes, so they were dropped.)
+// Kernels and launch forms.
+//  - pack_ring_kernel (G <= 1024, rows short enough for a two-stage ring;
+//    every DiT shape): persistent CTAs, several per SM, each streaming blocks of whole
+//    rows into its own shared-memory ring by bulk copies ahead of the
+//    arithmetic; the ring shape (CTAs per SM, rows per stage) is chosen by
+//    row length.
+//  - pack_g256_kernel (G <= 1024, longer rows): registers loaded straight
+//    from global memory with streaming 16-byte loads; a row longer than one
+//    CTA holds is split over a thread-block cluster, whose CTAs exchange
+//    their partial row maxima through distributed shared memory.
+//  - pack_kernel (G = 4096): the generic layout above (D, Walsh-Hadamard
+//    butterflies, Pi at the store), launched like pack_g256_kernel.
+// Both G <= 1024 kernels use the fixed tile layout described further down,
+// which applies H4 along each base-4 digit directly instead of the generic
+// butterflies.
 #include <cuda_bf16.h>
 
 #include "../../include/convrot.h"

@@ -1,7 +1,17 @@
-"""convrot_linear_lora_noalloc: the LoRA linear with T_ext in the library's
-static device scratch. Two calls in a row (different shapes and ranks, so the
-second reuses scratch the first wrote) must equal the two-call path with a
-caller-provided T_ext, bit for bit: the same kernels run on the same inputs."""
+"""convrot_linear_lora_noalloc: the LoRA linear in one call that allocates no
+device memory. It is for callers that must not call cudaMalloc: a plug-in
+whose host application owns all device memory through its own pool, a
+latency-bound loop that cannot pay for an allocation (or the synchronization
+a free brings), or code held to a device-memory budget fixed at load time.
+T_ext then lives in a 32 MiB array that the library declares at file scope
+on each device.
+
+Two calls in a row, with different shapes and ranks so that the second
+overwrites what the first left in the shared array, must equal the existing
+two-call path (convrot_lora_down into a caller-allocated T_ext, then
+convrot_linear_lora) bit for bit: the same kernels run on the same inputs.
+Requests larger than the array are refused before any launch. This file is
+named to be collected last."""
 
 import ctypes
 
@@ -49,6 +59,7 @@ def _case(rng, m, n, k, r):
 
 @pytest.mark.gpu
 def test_noalloc_lora_linear_twice_equals_two_call_path():
+    cbuild.build()
     rng = np.random.default_rng(2024)
     cases = [(_case(rng, 300, 512, 1024, 64), 64, cr.ACT_NONE), (_case(rng, 129, 256, 512, 32), 32, cr.ACT_GELU_ERF)]
     outs = []
