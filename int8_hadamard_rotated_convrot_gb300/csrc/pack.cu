@@ -434,9 +434,13 @@ __device__ __forceinline__ float absmax_g256(const float4 (&v)[16])
 }
 
 // Codes of slots j < nv. q0 is the thread's slot-0 quad (tile * QUADS + l); inv
-// the multiplier from scale_of.
+// the multiplier from scale_of. Register j holds slot j ^ sw (sw = 0 or 1, see
+// the ring kernel); the rotation commutes with that relabeling, because it
+// only swaps values along slot digit 2 and y_i = s - 2 x_{3-i} maps i -> i ^ 1
+// onto itself.
 template <int N, bool kBf16>
-__device__ __forceinline__ void store_g256(const float4 (&v)[16], int nv, int l, int q0, char *qrow, float inv)
+__device__ __forceinline__ void store_g256(const float4 (&v)[16], int nv, int l, int q0, char *qrow, float inv,
+                                           int sw = 0)
 {
     constexpr int LB = Tile<N>::LB, LANES = Tile<N>::LANES;
     // the kept value's sign times D1 at the output, for each lane digit
@@ -447,22 +451,26 @@ __device__ __forceinline__ void store_g256(const float4 (&v)[16], int nv, int l,
     if constexpr (N >= 2) lo = lane_out(l & 3) | (l & ~3);
     if constexpr (LB == 4) lo = lane_out(l & 3) | (lane_out((l >> 2) & 3) << 2);
     const int qo = q0 - l + lo;
+    // slot j ^ sw is j + sw for even j and j - sw for odd j
+    const int qe = qo + LANES * sw, qd = qo - LANES * sw;
+    const int nve = nv - sw, nvd = nv + sw;
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
-        if (j >= nv) break;
+        if (j >= ((j & 1) ? nvd : nve)) continue;
+        const int qj = ((j & 1) ? qd : qe) + LANES * j;
         const float r0 = code_of(v[j].x, inv, half_bits), r1 = code_of(v[j].y, inv, half_bits);
         const float r2 = code_of(v[j].z, inv, half_bits), r3 = code_of(v[j].w, inv, half_bits);
         if constexpr (kBf16) {
             // |r| <= 127: the bf16 of r is the top half of its fp32 bits (a zero code may be -0)
             const uint32_t lo = __byte_perm(__float_as_uint(r0), __float_as_uint(r1), 0x7632);
             const uint32_t hi = __byte_perm(__float_as_uint(r2), __float_as_uint(r3), 0x7632);
-            reinterpret_cast<uint2 *>(qrow)[qo + LANES * j] = make_uint2(lo, hi);
+            reinterpret_cast<uint2 *>(qrow)[qj] = make_uint2(lo, hi);
         } else {
             // r + 1.5 * 2^23 holds r in its low mantissa bits: the low byte is r as int8
             constexpr float kMagic = 12582912.0f;
             const uint32_t w0 = __float_as_uint(r0 + kMagic), w1 = __float_as_uint(r1 + kMagic);
             const uint32_t w2 = __float_as_uint(r2 + kMagic), w3 = __float_as_uint(r3 + kMagic);
-            reinterpret_cast<uint32_t *>(qrow)[qo + LANES * j] =
+            reinterpret_cast<uint32_t *>(qrow)[qj] =
                 __byte_perm(__byte_perm(w0, w1, 0x0040), __byte_perm(w2, w3, 0x0040), 0x5410);
         }
     }
@@ -546,9 +554,15 @@ __global__ void __launch_bounds__(512) pack_g256_kernel(PackArgs a, DirectPlan L
 
 // Ring form: persistent CTAs, several per SM, each streaming blocks of whole
 // rows into its own shared-memory ring by bulk copies (cp.async.bulk, one per
-// row, completion counted in bytes on the stage's mbarrier), stages - 1
-// blocks ahead of the arithmetic. CTAs on one SM drift out of phase, so the
-// copies of some overlap the arithmetic and stores of others.
+// row, completion counted in bytes on the stage's mbarrier). A stage is
+// refilled as soon as every thread has its block in registers, so all stages
+// are in flight while a block is rotated and stored. CTAs on one SM drift out
+// of phase, so the copies of some overlap the arithmetic and stores of others.
+//
+// Shared-memory banks. With 4 lanes per tile, one slot of a tile is 64
+// contiguous bytes and tiles sit 1 KB apart, so the 8 threads that a 16-byte
+// load serves at once (two tiles) would hit the same 16 banks. Odd tiles
+// therefore keep slot j ^ 1 in register j: the pair then covers all 32 banks.
 constexpr int kMaxStages = 8;
 
 struct RingPlan {
@@ -603,25 +617,25 @@ __global__ void __launch_bounds__(512) pack_ring_kernel(PackArgs a, RingPlan P)
     };
 
     if (threadIdx.x == 0)
-        for (int s = 0; s < NS - 1; ++s) issue(s, blockIdx.x + static_cast<int64_t>(s) * gridDim.x);
+        for (int s = 0; s < NS; ++s) issue(s, blockIdx.x + static_cast<int64_t>(s) * gridDim.x);
 
+    constexpr int LANES = Tile<N>::LANES;
+    const int sw = LB == 2 ? (t_row >> LB) & 1 : 0;  // odd tiles hold slot j ^ 1 in register j
+    const int nve = nv - sw, nvd = nv + sw;
     int it = 0;
     bool ok = true;
     for (int64_t blk = blockIdx.x; blk < nblocks; blk += gridDim.x, ++it) {
         const int stage = it % NS;
-        if (threadIdx.x == 0) {
-            // the stage refilled here was read into registers before the previous barrier
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            issue((it + NS - 1) % NS, blk + static_cast<int64_t>(NS - 1) * gridDim.x);
-        }
         const bool got = mbar_wait(bar_base + 8u * stage, static_cast<uint32_t>(it / NS) & 1u);
         const int64_t row = blk * R + r_local;
         const bool row_ok = got && row < a.rows;
         const float4 *src = reinterpret_cast<const float4 *>(ring + stage * P.stage_bytes + r_local * P.row_bytes) + q0;
+        const float4 *src_e = src + LANES * sw, *src_d = src - LANES * sw;
         float4 v[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j)
-            v[j] = (row_ok && j < nv) ? src[Tile<N>::LANES * j] : make_float4(0.f, 0.f, 0.f, 0.f);
+            v[j] = (row_ok && j < ((j & 1) ? nvd : nve)) ? ((j & 1) ? src_d : src_e)[LANES * j]
+                                                         : make_float4(0.f, 0.f, 0.f, 0.f);
         rotate_g256<N>(v, l);
         float *pp = part[it & 1];
         row_max_write(absmax_g256(v), tpr, pp);
@@ -630,12 +644,17 @@ __global__ void __launch_bounds__(512) pack_ring_kernel(PackArgs a, RingPlan P)
             ok = false;
             break;
         }
+        if (threadIdx.x == 0) {
+            // every thread read this stage into registers before the barrier: refill it now
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            issue(stage, blk + static_cast<int64_t>(NS) * gridDim.x);
+        }
         float inv;
         const float s = scale_of(row_max_read(tpr, r_local, pp), N, &inv);
         if (row < a.rows) {
             if (t_row == 0) a.scale[row] = s;
             char *qrow = static_cast<char *>(a.q) + row * a.ldq * (kBf16 ? 2 : 1);
-            store_g256<N, kBf16>(v, nv, l, q0, qrow, inv);
+            store_g256<N, kBf16>(v, nv, l, q0, qrow, inv, sw);
             zero_pad<kBf16>(qrow, kq, kpq, t_row, tpr);
         }
     }
