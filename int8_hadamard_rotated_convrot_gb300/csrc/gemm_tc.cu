@@ -19,8 +19,9 @@
 // Main form, gemm_tc_pair_kernel (m > 128): a CTA pair (cluster of 2,
 // tcgen05 cta_group::2), persistent over 256 x 256 output tiles.
 //   warp 0      TMA producer of each CTA: 64-wide K slices of its 128 rows of
-//               A and 128 rows of B, 128-byte swizzled, into a 5-stage ring;
-//               both CTAs' copies complete on the even CTA's barrier.
+//               A and 128 rows of B, 128-byte swizzled, into a ring of as many
+//               32 KB stages as fit beside the Y staging (6 for 256-wide
+//               tiles); both CTAs' copies complete on the even CTA's barrier.
 //   warp 1      allocates 512 TMEM columns (two 128 x 256 fp32 buffers per
 //               CTA); in the even CTA one thread issues tcgen05.mma (M = 256,
 //               N = 256, K = 16) over both CTAs' shared memory.
@@ -492,8 +493,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 // CTA of the pair issues M = 256, N = 256 MMAs that read both CTAs' shared
 // memory and write each CTA's 128 accumulator rows into that CTA's TMEM.
 // Per flop this moves two thirds of the single-CTA kernel's L2 traffic and
-// keeps six K slices in flight instead of four. The exact-chunk integer
-// accumulation and the epilogue are the same as above.
+// keeps six K slices in flight instead of three. The exact-chunk integer
+// accumulation is the same as above; the epilogue has sixteen warps (below).
 namespace pair {
 
 constexpr int BMC = 128;  // rows of A and D per CTA (256 per pair)
