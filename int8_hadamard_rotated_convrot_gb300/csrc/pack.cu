@@ -47,7 +47,9 @@
 //    butterflies, Pi at the store), launched like pack_g256_kernel.
 // Both G <= 1024 kernels use the fixed tile layout described further down,
 // which applies H4 along each base-4 digit directly instead of the generic
-// butterflies.
+// butterflies. The ring kernel at G = 1024 first applies digits 0-2 to 64
+// consecutive elements per thread and writes them back in place, so that no
+// digit needs lane shuffles (two-phase rotation, further down).
 #include <cuda_bf16.h>
 
 #include "../../include/convrot.h"
@@ -438,18 +440,24 @@ __device__ __forceinline__ float absmax_g256(const float4 (&v)[16])
 // the ring kernel); the rotation commutes with that relabeling, because it
 // only swaps values along slot digit 2 and y_i = s - 2 x_{3-i} maps i -> i ^ 1
 // onto itself.
-template <int N, bool kBf16>
+// kLaneDigits: the lane digits were applied by the sign-carrying shuffle
+// butterflies (their last sign, D1 and P are applied here); without it every
+// value already sits at its own place with its true sign.
+template <int N, bool kBf16, bool kLaneDigits = true>
 __device__ __forceinline__ void store_g256(const float4 (&v)[16], int nv, int l, int q0, char *qrow, float inv,
                                            int sw = 0)
 {
     constexpr int LB = Tile<N>::LB, LANES = Tile<N>::LANES;
-    // the kept value's sign times D1 at the output, for each lane digit
-    if constexpr (N >= 2) inv *= lane_c1(l & 3);
-    if constexpr (LB == 4) inv *= lane_c1((l >> 2) & 3);
+    int lo = l;
+    if constexpr (kLaneDigits) {
+        // the kept value's sign times D1 at the output, for each lane digit
+        if constexpr (N >= 2) inv *= lane_c1(l & 3);
+        if constexpr (LB == 4) inv *= lane_c1((l >> 2) & 3);
+        // P on each lane digit
+        if constexpr (N >= 2) lo = lane_out(l & 3) | (l & ~3);
+        if constexpr (LB == 4) lo = lane_out(l & 3) | (lane_out((l >> 2) & 3) << 2);
+    }
     const uint32_t half_bits = 0x3f000000u | (__float_as_uint(inv) & kSign);
-    int lo = l;  // P on each lane digit
-    if constexpr (N >= 2) lo = lane_out(l & 3) | (l & ~3);
-    if constexpr (LB == 4) lo = lane_out(l & 3) | (lane_out((l >> 2) & 3) << 2);
     const int qo = q0 - l + lo;
     // slot j ^ sw is j + sw for even j and j - sw for odd j
     const int qe = qo + LANES * sw, qd = qo - LANES * sw;
@@ -552,6 +560,60 @@ __global__ void __launch_bounds__(512) pack_g256_kernel(PackArgs a, DirectPlan L
     if (cl > 1) cluster_sync_all();  // no CTA leaves while another may still read its cta_max
 }
 
+// H4 along the slot digit held by slot bits 0-1 (slots 4 b + (0..3)) or by
+// slot bits 2-3 (slots b + 4 (0..3)), on every component.
+__device__ __forceinline__ void h4_slots_lo(float4 (&v)[16])
+{
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+        float4 &p0 = v[4 * b], &p1 = v[4 * b + 1], &p2 = v[4 * b + 2], &p3 = v[4 * b + 3];
+        h4_regs(p0.x, p1.x, p2.x, p3.x);
+        h4_regs(p0.y, p1.y, p2.y, p3.y);
+        h4_regs(p0.z, p1.z, p2.z, p3.z);
+        h4_regs(p0.w, p1.w, p2.w, p3.w);
+    }
+}
+
+__device__ __forceinline__ void h4_slots_hi(float4 (&v)[16])
+{
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+        float4 &p0 = v[b], &p1 = v[b + 4], &p2 = v[b + 8], &p3 = v[b + 12];
+        h4_regs(p0.x, p1.x, p2.x, p3.x);
+        h4_regs(p0.y, p1.y, p2.y, p3.y);
+        h4_regs(p0.z, p1.z, p2.z, p3.z);
+        h4_regs(p0.w, p1.w, p2.w, p3.w);
+    }
+}
+
+// Two-phase rotation, G >= 64 (n >= 3; used for G = 1024). Phase 1: a thread holds 64
+// consecutive elements of its row (16 consecutive quads: digit 0 the
+// component, digit 1 slot bits 0-1, digit 2 slot bits 2-3) and applies those
+// three digits in registers. Phase 2, after the values are written back in
+// place: the tile layout, whose slot digits are digit 3 (G <= 256: slot bits
+// 2-3) or digits 3 and 4 (G = 1024: slot bits 0-1 and 2-3). Every digit uses
+// the mirror form of 2 H4, so no lane shuffles, signs or output permutation
+// are involved, and each output sits at its own place.
+template <int N>
+__device__ __forceinline__ void rotate_chunk(float4 (&v)[16])
+{
+#pragma unroll
+    for (int j = 0; j < 16; ++j) h4_regs(v[j].x, v[j].y, v[j].z, v[j].w);  // digit 0
+    h4_slots_lo(v);                                                          // digit 1
+    h4_slots_hi(v);                                                          // digit 2
+}
+
+template <int N>
+__device__ __forceinline__ void rotate_tile_upper(float4 (&v)[16])
+{
+    if constexpr (Tile<N>::LB == 4) {
+        h4_slots_lo(v);  // digit 3
+        h4_slots_hi(v);  // digit 4
+    } else if constexpr (N >= 4) {
+        h4_slots_hi(v);  // digit 3
+    }
+}
+
 // Ring form: persistent CTAs, several per SM, each streaming blocks of whole
 // rows into its own shared-memory ring by bulk copies (cp.async.bulk, one per
 // row, completion counted in bytes on the stage's mbarrier). A stage is
@@ -575,9 +637,10 @@ struct RingPlan {
 
 using tc::mbar_wait;
 
-template <int N, bool kBf16>
+template <int N, bool kBf16, bool kTwoPhase>
 __global__ void __launch_bounds__(512) pack_ring_kernel(PackArgs a, RingPlan P)
 {
+    static_assert(!kTwoPhase || N >= 3, "the two-phase rotation needs whole 64-element chunks per group");
     extern __shared__ __align__(128) uint8_t ring[];
     __shared__ __align__(8) uint64_t full_bar[kMaxStages];
     __shared__ float part[2][128];
@@ -622,6 +685,12 @@ __global__ void __launch_bounds__(512) pack_ring_kernel(PackArgs a, RingPlan P)
     constexpr int LANES = Tile<N>::LANES;
     const int sw = LB == 2 ? (t_row >> LB) & 1 : 0;  // odd tiles hold slot j ^ 1 in register j
     const int nve = nv - sw, nvd = nv + sw;
+    // phase 1 of the two-phase rotation: register j holds quad j ^ csw of the
+    // thread's 16-quad chunk, so the 8 threads of a 16-byte load (chunks 256 B
+    // apart) hit 8 different bank groups; the rotation commutes with that
+    // relabeling (it xors digit 1 and the low bit of digit 2)
+    const int csw = t_row & 7;
+    const bool chunk_in = 16 * t_row < kq;  // whole chunks: kq is a multiple of G / 4 >= 16
     int it = 0;
     bool ok = true;
     for (int64_t blk = blockIdx.x; blk < nblocks; blk += gridDim.x, ++it) {
@@ -629,16 +698,34 @@ __global__ void __launch_bounds__(512) pack_ring_kernel(PackArgs a, RingPlan P)
         const bool got = mbar_wait(bar_base + 8u * stage, static_cast<uint32_t>(it / NS) & 1u);
         const int64_t row = blk * R + r_local;
         const bool row_ok = got && row < a.rows;
-        const float4 *src = reinterpret_cast<const float4 *>(ring + stage * P.stage_bytes + r_local * P.row_bytes) + q0;
-        const float4 *src_e = src + LANES * sw, *src_d = src - LANES * sw;
+        float4 *rowp = reinterpret_cast<float4 *>(ring + stage * P.stage_bytes + r_local * P.row_bytes);
         float4 v[16];
+        if constexpr (kTwoPhase) {
+            float4 *pc = rowp + 16 * t_row;
+            if (row_ok && chunk_in) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) v[j] = pc[j ^ csw];
+                rotate_chunk<N>(v);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) pc[j ^ csw] = v[j];
+            }
+            __syncthreads();
+        }
+        const float4 *src = rowp + q0;
+        const float4 *src_e = src + LANES * sw, *src_d = src - LANES * sw;
 #pragma unroll
         for (int j = 0; j < 16; ++j)
             v[j] = (row_ok && j < ((j & 1) ? nvd : nve)) ? ((j & 1) ? src_d : src_e)[LANES * j]
                                                          : make_float4(0.f, 0.f, 0.f, 0.f);
-        rotate_g256<N>(v, l);
+        if constexpr (kTwoPhase)
+            rotate_tile_upper<N>(v);
+        else
+            rotate_g256<N>(v, l);
         float *pp = part[it & 1];
         row_max_write(absmax_g256(v), tpr, pp);
+        // the stage's generic-proxy writes (phase 1) and reads come before the
+        // bulk copy that refills it
+        if constexpr (kTwoPhase) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         // every thread agrees on whether the stage arrived; a failed wait ends the loop everywhere
         if (!__syncthreads_and(got)) {
             ok = false;
@@ -654,7 +741,7 @@ __global__ void __launch_bounds__(512) pack_ring_kernel(PackArgs a, RingPlan P)
         if (row < a.rows) {
             if (t_row == 0) a.scale[row] = s;
             char *qrow = static_cast<char *>(a.q) + row * a.ldq * (kBf16 ? 2 : 1);
-            store_g256<N, kBf16>(v, nv, l, q0, qrow, inv, sw);
+            store_g256<N, kBf16, !kTwoPhase>(v, nv, l, q0, qrow, inv, sw);
             zero_pad<kBf16>(qrow, kq, kpq, t_row, tpr);
         }
     }
@@ -811,7 +898,9 @@ template <int N, bool kBf16>
 cudaError_t launch_g256(const PackArgs &a, cudaStream_t stream)
 {
     const RingLaunch L = ring_plan(a.k, Tile<N>::LB);
-    if (L.ctas_per_sm > 0) return launch_ring(pack_ring_kernel<N, kBf16>, L, a, stream);
+    // the two-phase rotation replaces two shuffle digits for G = 1024 (19.6 -> 18.1 us
+    // at K = 3072); for G = 64 and 256, one shuffle digit, it measured no faster
+    if (L.ctas_per_sm > 0) return launch_ring(pack_ring_kernel<N, kBf16, (N == 5)>, L, a, stream);
     return launch_plan(pack_g256_kernel<N, kBf16>, Shape{Tile<N>::LB, 16}, a, stream);
 }
 
