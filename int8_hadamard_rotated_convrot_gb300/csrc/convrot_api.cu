@@ -166,13 +166,15 @@ struct LoraArgs {
     int64_t ldt = 0;
     const void *b = nullptr;
     int64_t ldb = 0;
+    bool t_is_scratch = false;  // T_ext is the library's static scratch (non-null, 256-byte aligned)
 };
 
 bool lora_rank_ok(int32_t r) { return r >= 16 && r <= 256 && r % 16 == 0; }
 
-convrot_status run_gemm(const convrot_packed *x, const convrot_packed *w, const float *bias, float *Y,
-                        int32_t *A, int64_t ld, int32_t act, int32_t *dev_status, cudaStream_t stream,
-                        const LoraArgs &lora = LoraArgs{})
+// Host-side checks of a GEMM request; CONVROT_OK means run_gemm launches.
+convrot_status check_gemm(const convrot_packed *x, const convrot_packed *w, const float *bias, float *Y,
+                          int32_t *A, int64_t ld, int32_t act, int32_t *dev_status,
+                          const LoraArgs &lora = LoraArgs{})
 {
     if (act < CONVROT_ACT_NONE || act > CONVROT_ACT_GELU_TANH) return CONVROT_ERR_INVALID_ARG;
     convrot_status st = check_pair(x, w);
@@ -185,8 +187,9 @@ convrot_status run_gemm(const convrot_packed *x, const convrot_packed *w, const 
         const int64_t cols = (3 * int64_t{lora.r} + 63) / 64 * 64;
         if (lora.ldt < cols || lora.ldb < cols) return CONVROT_ERR_INVALID_ARG;
         if (m > 0 && n > 0) {
-            if (!lora.t || !lora.b) return CONVROT_ERR_INVALID_ARG;
-            if (!aligned(lora.t, 16) || !aligned(lora.b, 16) || lora.ldt % 8 || lora.ldb % 8)
+            if (!lora.b || (!lora.t_is_scratch && !lora.t)) return CONVROT_ERR_INVALID_ARG;
+            if ((!lora.t_is_scratch && !aligned(lora.t, 16)) || !aligned(lora.b, 16) || lora.ldt % 8 ||
+                lora.ldb % 8)
                 return CONVROT_ERR_ALIGNMENT;
         }
     }
@@ -196,9 +199,18 @@ convrot_status run_gemm(const convrot_packed *x, const convrot_packed *w, const 
         if (!aligned(out, 16) || ld % 4 != 0) return CONVROT_ERR_ALIGNMENT;
         if (bias && !aligned(bias, 4)) return CONVROT_ERR_ALIGNMENT;
         if (dev_status && !aligned(dev_status, 4)) return CONVROT_ERR_ALIGNMENT;
-    } else {
-        return CONVROT_OK;
     }
+    return CONVROT_OK;
+}
+
+convrot_status run_gemm(const convrot_packed *x, const convrot_packed *w, const float *bias, float *Y,
+                        int32_t *A, int64_t ld, int32_t act, int32_t *dev_status, cudaStream_t stream,
+                        const LoraArgs &lora = LoraArgs{})
+{
+    const convrot_status st = check_gemm(x, w, bias, Y, A, ld, act, dev_status, lora);
+    if (st != CONVROT_OK) return st;
+    const int64_t m = x->rows, n = w->rows;
+    if (m == 0 || n == 0) return CONVROT_OK;
     convrot::GemmArgs g{};
     g.qx = x->q;
     g.ldqx = x->ldq;
@@ -327,9 +339,18 @@ convrot_status convrot_linear_lora_noalloc(const convrot_packed *x, const convro
     if (x->rows > CONVROT_NOALLOC_SCRATCH_BYTES / (cols * 2)) return CONVROT_ERR_SCRATCH;
     if (x->rows == 0 || w->rows == 0) return convrot_linear_lora(x, w, bias, act, nullptr, cols, B_ext, lde, r, Y, ldy,
                                                                  dev_status, stream);
+    // every check of the linear comes before the first launch, as for the other entry points
+    LoraArgs lora;
+    lora.r = r;
+    lora.ldt = cols;
+    lora.b = B_ext;
+    lora.ldb = lde;
+    lora.t_is_scratch = true;
+    convrot_status st = check_gemm(x, w, bias, Y, nullptr, ldy, act, dev_status, lora);
+    if (st != CONVROT_OK) return st;
     void *scratch = noalloc_scratch_address();
     if (!scratch) return CONVROT_ERR_CUDA;
-    convrot_status st = convrot_lora_down(X, x->rows, x->k, ldx, A_ext, r, lda, scratch, cols, dev_status, stream);
+    st = convrot_lora_down(X, x->rows, x->k, ldx, A_ext, r, lda, scratch, cols, dev_status, stream);
     if (st != CONVROT_OK) return st;
     return convrot_linear_lora(x, w, bias, act, scratch, cols, B_ext, lde, r, Y, ldy, dev_status, stream);
 }

@@ -100,14 +100,18 @@ def test_pack_matches_oracle(G, k, codes):
 
 
 @pytest.mark.parametrize("G,k,m", [(256, 768, 3000), (4, 768, 3000), (64, 16384, 700), (256, 28672, 40),
-                                   (1024, 3072, 3000), (1024, 16384, 500), (1024, 28672, 40)],
+                                   (1024, 3072, 3000), (1024, 16384, 500), (1024, 28672, 40),
+                                   (1024, 1024, 999), (1024, 2048, 777), (1024, 5120, 301)],
                          ids=["ring-wraps", "ring-wraps-G4", "ring-one-cta-per-sm", "direct",
-                              "G1024-ring", "G1024-ring-one-cta", "G1024-direct"])
+                              "G1024-ring", "G1024-ring-one-cta", "G1024-direct",
+                              "G1024-ring-4-row-stages", "G1024-ring-2-row-stages", "G1024-ring-k5120"])
 @pytest.mark.parametrize("codes", CODES, ids=CODE_IDS)
 def test_pack_launch_forms(G, k, m, codes):
     """Each launch form of the G <= 1024 pack: a shared-memory ring that wraps many
-    times, a ring of one CTA per SM (long rows), and the direct form; G = 1024
-    uses 16-lane tiles with two lane digits."""
+    times, a ring of one CTA per SM (long rows), and the direct form. G = 1024
+    uses 16-lane tiles; in the ring it takes the two-phase rotation (64-element
+    chunks written back in place, then the tile layout), here with 1-, 2- and
+    4-row stages and 2 or 3 stages."""
     rng = np.random.default_rng(G + k + m)
     X = special_rows(rng, m, k)
     p = gpu_pack(X, G, codes)

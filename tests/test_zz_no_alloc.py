@@ -42,6 +42,29 @@ def test_noalloc_rejects_requests_beyond_the_scratch():
                                            cols, 20, FAKE, 8, None, None) == cr.ERR_INVALID_ARG
 
 
+def test_noalloc_checks_the_linear_before_any_device_work():
+    """The linear's own argument errors come back before the scratch lookup and
+    before the down kernel would run (here, without a GPU, any device call would
+    answer CONVROT_ERR_CUDA instead)."""
+    cbuild.build()
+    lib = cr.load()
+    r = 64
+    cols = lib.convrot_lora_cols(r)
+    ld = cr.convrot_ldq(256)
+    args = lambda x, w, ldy, Y: (ctypes.byref(x), ctypes.byref(w), None, 0, FAKE, 256, FAKE, 256, FAKE, cols, r,
+                                 Y, ldy, None, None)
+    x = cr._Packed(FAKE, FAKE, 8, 256, ld, 256, cr.CODES_I8)
+    w = cr._Packed(FAKE, FAKE, 8, 256, ld, 256, cr.CODES_I8)
+    assert lib.convrot_linear_lora_noalloc(*args(x, w, 8, FAKE)) == cr.ERR_UNSUPPORTED  # I8 codes: no LoRA chunk
+    x = cr._Packed(FAKE, FAKE, 8, 256, ld, 256, cr.CODES_BF16)
+    w = cr._Packed(FAKE, FAKE, 8, 256, ld, 256, cr.CODES_BF16)
+    assert lib.convrot_linear_lora_noalloc(*args(x, w, 8, FAKE + 4)) == cr.ERR_ALIGNMENT  # Y not 16-byte aligned
+    assert lib.convrot_linear_lora_noalloc(*args(x, w, 7, FAKE)) == cr.ERR_INVALID_ARG  # ldy < n
+    assert lib.convrot_linear_lora_noalloc(*args(x, w, 8, None)) == cr.ERR_INVALID_ARG  # no Y
+    w_other_g = cr._Packed(FAKE, FAKE, 8, 256, ld, 64, cr.CODES_BF16)
+    assert lib.convrot_linear_lora_noalloc(*args(x, w_other_g, 8, FAKE)) == cr.ERR_GROUP_SIZE
+
+
 def _case(rng, m, n, k, r):
     X = rng.standard_normal((m, k)).astype(np.float32)
     W = (0.02 * rng.standard_normal((n, k))).astype(np.float32)
