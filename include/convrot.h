@@ -48,7 +48,7 @@ typedef enum {
     CONVROT_ERR_K_RANGE = 4,     /* k < 1 or k > CONVROT_MAX_K */
     CONVROT_ERR_CUDA = 5,        /* a kernel launch failed */
     CONVROT_ERR_TIMEOUT = 6,     /* written to *dev_status by a kernel whose bounded wait ran out */
-    CONVROT_ERR_UNSUPPORTED = 7, /* valid request this build has no kernel for */
+    CONVROT_ERR_UNSUPPORTED = 7, /* valid request that no kernel of the library supports */
     CONVROT_ERR_SCRATCH = 8      /* larger than the static scratch of convrot_linear_lora_noalloc */
 } convrot_status;
 

@@ -379,7 +379,7 @@ const char *convrot_status_string(convrot_status s)
     case CONVROT_ERR_K_RANGE: return "k must be in [1, 133144]";
     case CONVROT_ERR_CUDA: return "CUDA launch failed";
     case CONVROT_ERR_TIMEOUT: return "a kernel gave up a bounded wait";
-    case CONVROT_ERR_UNSUPPORTED: return "no kernel for this request in this build";
+    case CONVROT_ERR_UNSUPPORTED: return "valid request that no kernel of the library supports (e.g. LoRA with I8 codes)";
     case CONVROT_ERR_SCRATCH: return "request larger than the static scratch of the no-allocation entry point";
     default: return "unknown status";
     }
