@@ -216,6 +216,10 @@ def run_reference(args):
     from int8_hadamard_rotated_convrot_gb300 import inputs
 
     wl = inputs.WORKLOADS[args.workload]
+    if world > 1:
+        # torch.distributed.run sets OMP_NUM_THREADS=1 in every rank; rank 0 is the only
+        # one working here, so the oracle gets this process's cores (read before it loads)
+        os.environ["OMP_NUM_THREADS"] = str(len(os.sched_getaffinity(0)))
     budget = max(1.0, min(args.cpu_seconds, 120.0 / max(args.steps + args.warmup, 1)))
     cb = cpu_baseline(wl, budget * (args.steps), steps=args.steps, warmup=args.warmup)
     line = {
@@ -465,7 +469,9 @@ def run_ours(args):
         "config": {"workload": workload_name(wl), "global_batch": wl.m * world,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "codes": "i8" if codes == cr.CODES_I8 else "bf16",
-                   "l2": f"{R} rotating input/output sets, {touched / 1e6:.0f} MB touched per step (> L2)",
+                   "l2": f"{R} rotating input/output sets, {touched / 1e6:.2f} MB touched per step "
+                         + ("(> L2)" if touched > L2_BYTES else
+                            "(all sets fit in L2: L2-warm timing, a parity-size workload)"),
                    "launch": ("eager, one C-ABI call per kernel" if graph is None else
                               "the K timed steps replayed as one CUDA graph of the same C-ABI launches"),
                    "kernel_timing": "each launch of the step repeated K times back to back over the rotating "

@@ -75,3 +75,5 @@ def test_reference_arm_under_torchrun_prints_once():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
     assert d["e2e"]["h2d_bytes_per_step"] == 0
+    # the launcher's OMP_NUM_THREADS=1 does not starve the only working rank
+    assert d["cpu_baseline"]["cores"] == len(os.sched_getaffinity(0))
