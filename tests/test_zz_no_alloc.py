@@ -94,3 +94,23 @@ def test_noalloc_lora_linear_twice_equals_two_call_path():
         torch.cuda.synchronize()
         assert torch.equal(y, y_ref)
         assert torch.isfinite(y).all() and y.abs().max() > 0
+
+
+@pytest.mark.gpu
+def test_noalloc_at_the_largest_accepted_request():
+    """r = 256 at the most rows the array holds (21845 x 768 bf16 fills all but 512
+    bytes of it): the last rows of T_ext sit at the array's end, and the result still
+    equals the two-call path; one more row is refused."""
+    cbuild.build()
+    r = 256
+    m = cr.NOALLOC_SCRATCH_BYTES // (cr.lora_cols(r) * 2)
+    assert m == 21845
+    rng = np.random.default_rng(77)
+    Xd, px, pw, b, A_ext, B_ext = _case(rng, m, 256, 256, r)
+    y = cr.convrot_linear_lora_noalloc(px, pw, b, cr.ACT_NONE, Xd, A_ext, B_ext, r)
+    y_ref = cr.convrot_linear_lora(px, pw, b, cr.ACT_NONE, cr.convrot_lora_down(Xd, A_ext), B_ext, r)
+    torch.cuda.synchronize()
+    assert torch.equal(y, y_ref)
+    Xd1, px1, pw1, b1, A1, B1 = _case(rng, m + 1, 256, 256, r)
+    with pytest.raises(cr.ConvrotError):
+        cr.convrot_linear_lora_noalloc(px1, pw1, b1, cr.ACT_NONE, Xd1, A1, B1, r)
