@@ -614,6 +614,116 @@ __device__ __forceinline__ void rotate_tile_upper(float4 (&v)[16])
     }
 }
 
+// Eight-lane tiles for the ring at G <= 256: a 256-element tile is 8 lanes x
+// 8 float4 slots, quad q = 8 j + l (slot j, lane l), element 4 q + c. Half the
+// registers of the 4-lane tile a thread, so twice the warps fit an SM.
+//   digit 0  the component c                        registers
+//   digit 1  lane bits 0-1                          sign-carrying shuffle butterflies
+//   digit 2  lane bit 2 (low) and slot bit 0 (high) one shuffle and one register butterfly
+//   digit 3  slot bits 1-2                          registers
+// Digit 2 uses 2 H4 = P D1 W1 D1 with W1 = H2 (x) H2: a radix-2 butterfly on
+// each of its two bits, D1 = -1 where both bits are set, P swapping the bits.
+// The input D1 folds into the butterfly coefficients (odd slots of lane-bit-0
+// threads come out of the shuffle butterfly negated, and the register
+// butterfly takes that sign as its coefficient); the output D1 goes into the
+// quantization multiplier of odd slots, P into the store address.
+template <int N>
+__device__ __forceinline__ void rotate_t8(float4 (&v)[8], int l)
+{
+#pragma unroll
+    for (int j = 0; j < 8; ++j) h4_regs(v[j].x, v[j].y, v[j].z, v[j].w);  // digit 0
+    if constexpr (N >= 2) {                                                 // digit 1
+        const float c0 = lane_c0(l & 3), c1 = lane_c1(l & 3);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            h4_lanes(v[j].x, c0, c1, 1, 2);
+            h4_lanes(v[j].y, c0, c1, 1, 2);
+            h4_lanes(v[j].z, c0, c1, 1, 2);
+            h4_lanes(v[j].w, c0, c1, 1, 2);
+        }
+    }
+    if constexpr (N >= 3) {  // digit 2
+        const float ce = (l & 4) ? -1.0f : 1.0f, co = -ce;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float c = (j & 1) ? co : ce;
+            v[j].x = fmaf(c, v[j].x, __shfl_xor_sync(kFull, v[j].x, 4));
+            v[j].y = fmaf(c, v[j].y, __shfl_xor_sync(kFull, v[j].y, 4));
+            v[j].z = fmaf(c, v[j].z, __shfl_xor_sync(kFull, v[j].z, 4));
+            v[j].w = fmaf(c, v[j].w, __shfl_xor_sync(kFull, v[j].w, 4));
+        }
+        // odd slots now carry the sign co: the register butterfly on slot bit 0
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            const float4 x = v[2 * b], y = v[2 * b + 1];
+            v[2 * b] = make_float4(fmaf(co, y.x, x.x), fmaf(co, y.y, x.y), fmaf(co, y.z, x.z), fmaf(co, y.w, x.w));
+            v[2 * b + 1] =
+                make_float4(fmaf(ce, y.x, x.x), fmaf(ce, y.y, x.y), fmaf(ce, y.z, x.z), fmaf(ce, y.w, x.w));
+        }
+    }
+    if constexpr (N >= 4) {  // digit 3: slots b + 2 (0..3)
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+            float4 &p0 = v[b], &p1 = v[b + 2], &p2 = v[b + 4], &p3 = v[b + 6];
+            h4_regs(p0.x, p1.x, p2.x, p3.x);
+            h4_regs(p0.y, p1.y, p2.y, p3.y);
+            h4_regs(p0.z, p1.z, p2.z, p3.z);
+            h4_regs(p0.w, p1.w, p2.w, p3.w);
+        }
+    }
+}
+
+template <int S>
+__device__ __forceinline__ float absmax_s(const float4 (&v)[S])
+{
+    float m = 0.0f;
+#pragma unroll
+    for (int j = 0; j < S; ++j)
+        m = fmaxf(m, fmaxf(fmaxf(fabsf(v[j].x), fabsf(v[j].y)), fmaxf(fabsf(v[j].z), fabsf(v[j].w))));
+    return m;
+}
+
+// Codes of slots j < nv of the eight-lane layout. tq is the tile's first quad.
+template <int N, bool kBf16>
+__device__ __forceinline__ void store_t8(const float4 (&v)[8], int nv, int l, int tq, char *qrow, float inv)
+{
+    int lo = l & 3;
+    if constexpr (N >= 2) {
+        inv *= lane_c1(l & 3);  // digit 1: the kept value's sign times D1
+        lo = lane_out(l & 3);   // digit 1: P
+    }
+    const int lb2 = (l >> 2) & 1;
+    float inv_o = inv;
+    int off_e = 4 * lb2 + lo, off_o = 8 + 4 * lb2 + lo;  // quad 8 j + l, per slot parity
+    if constexpr (N >= 3) {
+        if (lb2) inv_o = -inv;                 // digit 2: output D1 at both bits set
+        off_e = 8 * lb2 + lo;                  // digit 2: P swaps lane bit 2 (quad bit 2)
+        off_o = 8 * lb2 + 4 + lo;              // and slot bit 0 (quad bit 3)
+    }
+    const uint32_t half_e = 0x3f000000u | (__float_as_uint(inv) & kSign);
+    const uint32_t half_o = 0x3f000000u | (__float_as_uint(inv_o) & kSign);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        if (j >= nv) break;
+        const float m = (j & 1) ? inv_o : inv;
+        const uint32_t h = (j & 1) ? half_o : half_e;
+        const int q = tq + 8 * (j & 6) + ((j & 1) ? off_o : off_e);
+        const float r0 = code_of(v[j].x, m, h), r1 = code_of(v[j].y, m, h);
+        const float r2 = code_of(v[j].z, m, h), r3 = code_of(v[j].w, m, h);
+        if constexpr (kBf16) {
+            const uint32_t w01 = __byte_perm(__float_as_uint(r0), __float_as_uint(r1), 0x7632);
+            const uint32_t w23 = __byte_perm(__float_as_uint(r2), __float_as_uint(r3), 0x7632);
+            reinterpret_cast<uint2 *>(qrow)[q] = make_uint2(w01, w23);
+        } else {
+            constexpr float kMagic = 12582912.0f;
+            const uint32_t w0 = __float_as_uint(r0 + kMagic), w1 = __float_as_uint(r1 + kMagic);
+            const uint32_t w2 = __float_as_uint(r2 + kMagic), w3 = __float_as_uint(r3 + kMagic);
+            reinterpret_cast<uint32_t *>(qrow)[q] =
+                __byte_perm(__byte_perm(w0, w1, 0x0040), __byte_perm(w2, w3, 0x0040), 0x5410);
+        }
+    }
+}
+
 // Ring form: persistent CTAs, several per SM, each streaming blocks of whole
 // rows into its own shared-memory ring by bulk copies (cp.async.bulk, one per
 // row, completion counted in bytes on the stage's mbarrier). A stage is
@@ -637,10 +747,16 @@ struct RingPlan {
 
 using tc::mbar_wait;
 
-template <int N, bool kBf16, bool kTwoPhase>
-__global__ void __launch_bounds__(512) pack_ring_kernel(PackArgs a, RingPlan P)
+// Register layouts of the ring kernel.
+enum RingLayout { kLanes4 = 0, kTwoPhase4 = 1, kLanes8 = 2 };
+
+template <int N, bool kBf16, int kLayout>
+__global__ void __launch_bounds__(512) __maxnreg__(kLayout == 2 ? 80 : 128) pack_ring_kernel(PackArgs a, RingPlan P)
 {
+    constexpr bool kTwoPhase = kLayout == kTwoPhase4;
+    constexpr bool k8 = kLayout == kLanes8;
     static_assert(!kTwoPhase || N >= 3, "the two-phase rotation needs whole 64-element chunks per group");
+    static_assert(!k8 || N <= 4, "eight-lane tiles hold groups of up to 256");
     extern __shared__ __align__(128) uint8_t ring[];
     __shared__ __align__(8) uint64_t full_bar[kMaxStages];
     __shared__ float part[2][128];
@@ -649,10 +765,13 @@ __global__ void __launch_bounds__(512) pack_ring_kernel(PackArgs a, RingPlan P)
     const int r_local = threadIdx.x / tpr;
     const int t_row = threadIdx.x - r_local * tpr;
     const int kq = a.k >> 2, kpq = a.kpad >> 2;
-    constexpr int LB = Tile<N>::LB;
-    const int l = t_row & (Tile<N>::LANES - 1);
-    const int q0 = (t_row >> LB) * Tile<N>::QUADS + l;
-    const int nv = valid_slots<LB>(kq, q0);
+    constexpr int LB = k8 ? 3 : Tile<N>::LB;
+    constexpr int LANES = 1 << LB;
+    constexpr int SLOTS = k8 ? 8 : 16;
+    const int l = t_row & (LANES - 1);
+    const int tq = (t_row >> LB) * (SLOTS << LB);  // the tile's first quad
+    const int q0 = tq + l;
+    const int nv = k8 ? min(max((kq - q0 + 7) >> 3, 0), 8) : valid_slots<LB>(kq, q0);
     const int64_t nblocks = (a.rows + R - 1) / R;
     const uint32_t ring_base = static_cast<uint32_t>(__cvta_generic_to_shared(ring));
     const uint32_t bar_base = static_cast<uint32_t>(__cvta_generic_to_shared(full_bar));
@@ -682,7 +801,6 @@ __global__ void __launch_bounds__(512) pack_ring_kernel(PackArgs a, RingPlan P)
     if (threadIdx.x == 0)
         for (int s = 0; s < NS; ++s) issue(s, blockIdx.x + static_cast<int64_t>(s) * gridDim.x);
 
-    constexpr int LANES = Tile<N>::LANES;
     const int sw = LB == 2 ? (t_row >> LB) & 1 : 0;  // odd tiles hold slot j ^ 1 in register j
     const int nve = nv - sw, nvd = nv + sw;
     // phase 1 of the two-phase rotation: register j holds quad j ^ csw of the
@@ -699,7 +817,7 @@ __global__ void __launch_bounds__(512) pack_ring_kernel(PackArgs a, RingPlan P)
         const int64_t row = blk * R + r_local;
         const bool row_ok = got && row < a.rows;
         float4 *rowp = reinterpret_cast<float4 *>(ring + stage * P.stage_bytes + r_local * P.row_bytes);
-        float4 v[16];
+        float4 v[SLOTS];
         if constexpr (kTwoPhase) {
             float4 *pc = rowp + 16 * t_row;
             if (row_ok && chunk_in) {
@@ -712,17 +830,24 @@ __global__ void __launch_bounds__(512) pack_ring_kernel(PackArgs a, RingPlan P)
             __syncthreads();
         }
         const float4 *src = rowp + q0;
-        const float4 *src_e = src + LANES * sw, *src_d = src - LANES * sw;
+        if constexpr (k8) {
+            // a quarter-warp is one tile: 8 consecutive quads, no bank conflicts
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-            v[j] = (row_ok && j < ((j & 1) ? nvd : nve)) ? ((j & 1) ? src_d : src_e)[LANES * j]
-                                                         : make_float4(0.f, 0.f, 0.f, 0.f);
-        if constexpr (kTwoPhase)
-            rotate_tile_upper<N>(v);
-        else
-            rotate_g256<N>(v, l);
+            for (int j = 0; j < 8; ++j) v[j] = (row_ok && j < nv) ? src[8 * j] : make_float4(0.f, 0.f, 0.f, 0.f);
+            rotate_t8<N>(v, l);
+        } else {
+            const float4 *src_e = src + LANES * sw, *src_d = src - LANES * sw;
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                v[j] = (row_ok && j < ((j & 1) ? nvd : nve)) ? ((j & 1) ? src_d : src_e)[LANES * j]
+                                                             : make_float4(0.f, 0.f, 0.f, 0.f);
+            if constexpr (kTwoPhase)
+                rotate_tile_upper<N>(v);
+            else
+                rotate_g256<N>(v, l);
+        }
         float *pp = part[it & 1];
-        row_max_write(absmax_g256(v), tpr, pp);
+        row_max_write(absmax_s<SLOTS>(v), tpr, pp);
         // the stage's generic-proxy writes (phase 1) and reads come before the
         // bulk copy that refills it
         if constexpr (kTwoPhase) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -741,7 +866,10 @@ __global__ void __launch_bounds__(512) pack_ring_kernel(PackArgs a, RingPlan P)
         if (row < a.rows) {
             if (t_row == 0) a.scale[row] = s;
             char *qrow = static_cast<char *>(a.q) + row * a.ldq * (kBf16 ? 2 : 1);
-            store_g256<N, kBf16, !kTwoPhase>(v, nv, l, q0, qrow, inv, sw);
+            if constexpr (k8)
+                store_t8<N, kBf16>(v, nv, l, tq, qrow, inv);
+            else
+                store_g256<N, kBf16, !kTwoPhase>(v, nv, l, q0, qrow, inv, sw);
             zero_pad<kBf16>(qrow, kq, kpq, t_row, tpr);
         }
     }
@@ -844,25 +972,32 @@ struct RingTuning {
     int ctas_per_sm;
     uint32_t ring_bytes;
     int threads_target;
+    int min_stages;
 };
-constexpr RingTuning kRingTunings[] = {{4, 50 * 1024, 64}, {2, 100 * 1024, 128}, {1, 200 * 1024, 128}};
+constexpr RingTuning kRingTunings[] = {
+    {5, 25 * 1024, 64, 1}, {4, 50 * 1024, 64, 2}, {2, 100 * 1024, 128, 2}, {1, 200 * 1024, 128, 2}};
+// Eight-lane layout (half the registers a thread): twice the threads a row, so
+// the same rings hold twice the warps.
+constexpr RingTuning kRingTunings8[] = {{4, 50 * 1024, 192, 2}, {2, 100 * 1024, 384, 2}, {1, 200 * 1024, 512, 2}};
 
 struct RingLaunch {
     RingPlan P;
     int ctas_per_sm;  // 0: rows too long for a ring
 };
 
-RingLaunch ring_plan(int k, int lane_bits)
+template <size_t NT>
+RingLaunch ring_plan(int k, int lane_bits, const RingTuning (&tunings)[NT])
 {
-    const int T = threads_per_row(Shape{lane_bits, 16}, k);
+    const int T = threads_per_row(Shape{lane_bits, lane_bits == 3 ? 8 : 16}, k);
     const int step = 32 / gcd_int(T, 32);  // rows per stage must fill whole warps
     const uint64_t row_bytes = 4ull * static_cast<uint64_t>(k);
     if (step * T > 512) return RingLaunch{};
-    for (const RingTuning &tu : kRingTunings) {
+    for (const RingTuning &tu : tunings) {
         int R = step;
         while (R * T < tu.threads_target && (R + step) * T <= 512) R += step;
-        while (R > step && 2ull * R * row_bytes > tu.ring_bytes) R -= step;
-        if (2ull * R * row_bytes > tu.ring_bytes) continue;
+        const uint64_t ns_min = static_cast<uint64_t>(tu.min_stages);
+        while (R > step && ns_min * R * row_bytes > tu.ring_bytes) R -= step;
+        if (ns_min * R * row_bytes > tu.ring_bytes) continue;
         RingLaunch L{};
         L.ctas_per_sm = tu.ctas_per_sm;
         L.P.threads_per_row = T;
@@ -887,20 +1022,31 @@ cudaError_t launch_ring(Kernel kern, const RingLaunch &L, const PackArgs &a, cud
     const int smem = L.P.stages * static_cast<int>(L.P.stage_bytes);
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
+    const int threads = L.P.threads_per_row * L.P.rows_per_stage;
+    // a persistent grid must be resident at once: never plan more CTAs an SM than fit
+    int resident = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident, kern, threads, smem);
+    if (e != cudaSuccess) return e;
+    const int per_sm = resident > 0 && resident < L.ctas_per_sm ? resident : L.ctas_per_sm;
     const int64_t nblocks = (a.rows + L.P.rows_per_stage - 1) / L.P.rows_per_stage;
-    const int64_t slots = static_cast<int64_t>(sms) * L.ctas_per_sm;
+    const int64_t slots = static_cast<int64_t>(sms) * per_sm;
     const int64_t grid = nblocks < slots ? nblocks : slots;
-    kern<<<static_cast<unsigned>(grid), L.P.threads_per_row * L.P.rows_per_stage, smem, stream>>>(a, L.P);
+    kern<<<static_cast<unsigned>(grid), threads, smem, stream>>>(a, L.P);
     return cudaGetLastError();
 }
 
 template <int N, bool kBf16>
 cudaError_t launch_g256(const PackArgs &a, cudaStream_t stream)
 {
-    const RingLaunch L = ring_plan(a.k, Tile<N>::LB);
+    const RingLaunch L = ring_plan(a.k, Tile<N>::LB, kRingTunings);
     // the two-phase rotation replaces two shuffle digits for G = 1024 (19.6 -> 18.1 us
     // at K = 3072); for G = 64 and 256, one shuffle digit, it measured no faster
-    if (L.ctas_per_sm > 0) return launch_ring(pack_ring_kernel<N, kBf16, (N == 5)>, L, a, stream);
+    if constexpr (N <= 2) {
+        const RingLaunch L8 = ring_plan(a.k, 3, kRingTunings8);
+        if (L8.ctas_per_sm > 0) return launch_ring(pack_ring_kernel<N, kBf16, kLanes8>, L8, a, stream);
+    }
+    if (L.ctas_per_sm > 0)
+        return launch_ring(pack_ring_kernel<N, kBf16, N == 5 ? kTwoPhase4 : kLanes4>, L, a, stream);
     return launch_plan(pack_g256_kernel<N, kBf16>, Shape{Tile<N>::LB, 16}, a, stream);
 }
 
