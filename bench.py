@@ -392,7 +392,40 @@ def run_ours(args):
         b1.record(stream)
         torch.cuda.synchronize(dev)
         kern_ms[tag] = kern_ms.get(tag, 0.0) + b0.elapsed_time(b1) / args.steps
+        if tag == "pack" and "pack_first" not in kern_ms:
+            kern_ms["pack_first"] = b0.elapsed_time(b1) / args.steps
         del g
+    # Context for the pack's roofline: torch's own elementwise conversion of the same
+    # activations to the code type (the same bytes: 4 read and 1 or 2 written per
+    # element), timed the same way. Not part of a step and not counted in gpu_launches.
+    code_dtype = torch.int8 if codes == cr.CODES_I8 else torch.bfloat16
+    conv_out = [torch.empty((wl.m, wl.k), dtype=code_dtype, device=dev) for _ in range(R)]
+
+    def conv_batch():
+        for i in range(args.steps):
+            conv_out[i % R].copy_(Xs[i % R])
+    def conv_run(g):
+        with torch.cuda.stream(stream):
+            if g is not None:
+                g.replay()
+            else:
+                conv_batch()
+
+    conv_run(None)
+    g = None
+    if graph is not None:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            conv_batch()
+    conv_run(g)
+    torch.cuda.synchronize(dev)
+    b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    b0.record(stream)
+    conv_run(g)
+    b1.record(stream)
+    torch.cuda.synchronize(dev)
+    conv_ms = b0.elapsed_time(b1) / args.steps
+    del g, conv_out
     # keep the GPU busy a little longer with the same steps for the clock record
     t_keep = time.time()
     i = 0
@@ -457,6 +490,9 @@ def run_ours(args):
     gemm_tops = ops / (gemm_avg * 1e-3) / 1e12
     pack_bytes = sum(wl.m * (4 * st.k + code_b * st.k + 4) for st in stages)
     pack_gbs = pack_bytes / (pack_avg * 1e-3) / 1e9
+    first_pack_bytes = wl.m * (4 * stages[0].k + code_b * stages[0].k + 4)
+    first_pack_ms = kern_ms["pack_first"]
+    conv_gbs = wl.m * stages[0].k * (4 + code_b) / (conv_ms * 1e-3) / 1e9
     traffic = measured_traffic(wl.name, "i8" if codes == cr.CODES_I8 else "bf16")
 
     if rank != 0:
@@ -490,7 +526,13 @@ def run_ours(args):
                         if codes == cr.CODES_I8 else {})},
         "roofline_pack": {"bound": "hbm", "achieved": pack_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
                           "frac": pack_gbs / pk["hbm_gbs"], "bytes_per_launch": pack_bytes,
-                          "peak_source": f"{pk['source']} copy bandwidth"},
+                          "peak_source": f"{pk['source']} copy bandwidth",
+                          "same_bytes_conversion": {
+                              "what": f"torch fp32 -> {str(code_dtype).replace('torch.', '')} copy_ of the "
+                                      "same activations, timed like the pack (context, not a step kernel)",
+                              "ms": conv_ms, "gbs": conv_gbs,
+                              "pack_ms": first_pack_ms,
+                              "pack_gbs": first_pack_bytes / (first_pack_ms * 1e-3) / 1e9}},
         "e2e": {"value": job_tops(world, ops, e2e_ms), "unit": "TOPS",
                 "pipelining": "H2D of step i+1 and D2H of step i overlap compute on separate streams",
                 "h2d_bytes_per_step": wl.m * wl.k * 4, "d2h_bytes_per_step": wl.m * n_out * 4,
