@@ -34,22 +34,24 @@
 // butterflies). The float4 component is digit 0 of the in-group index.
 //
 // Kernels and launch forms.
-//  - pack_ring_kernel (G <= 1024, rows short enough for a two-stage ring;
-//    every DiT shape): persistent CTAs, several per SM, each streaming blocks of whole
+//  - pack_ring_kernel (G <= 1024, rows short enough for its rings; every DiT
+//    shape): persistent CTAs, several per SM, each streaming blocks of whole
 //    rows into its own shared-memory ring by bulk copies ahead of the
-//    arithmetic; the ring shape (CTAs per SM, rows per stage) is chosen by
-//    row length.
+//    arithmetic; the ring shape (CTAs per SM, rows per stage, stages) is
+//    chosen by row length, the grid by the CTAs that are resident at once.
 //  - pack_g256_kernel (G <= 1024, longer rows): registers loaded straight
 //    from global memory with streaming 16-byte loads; a row longer than one
 //    CTA holds is split over a thread-block cluster, whose CTAs exchange
 //    their partial row maxima through distributed shared memory.
 //  - pack_kernel (G = 4096): the generic layout above (D, Walsh-Hadamard
 //    butterflies, Pi at the store), launched like pack_g256_kernel.
-// Both G <= 1024 kernels use the fixed tile layout described further down,
-// which applies H4 along each base-4 digit directly instead of the generic
-// butterflies. The ring kernel at G = 1024 first applies digits 0-2 to 64
-// consecutive elements per thread and writes them back in place, so that no
-// digit needs lane shuffles (two-phase rotation, further down).
+// Both G <= 1024 kernels use fixed tile layouts (further down) that apply H4
+// along each base-4 digit directly instead of the generic butterflies. The
+// ring kernel has three register layouts: 4 lanes x 16 slots per 256-element
+// tile (G = 64, 256); 8 lanes x 8 slots (G <= 16: half the registers, twice
+// the warps); and at G = 1024 a two-phase rotation that first applies digits
+// 0-2 to 64 consecutive elements per thread and writes them back in place,
+// so that no digit needs lane shuffles.
 #include <cuda_bf16.h>
 
 #include "../../include/convrot.h"
