@@ -976,8 +976,7 @@ struct RingTuning {
     int threads_target;
     int min_stages;
 };
-constexpr RingTuning kRingTunings[] = {
-    {5, 25 * 1024, 64, 1}, {4, 50 * 1024, 64, 2}, {2, 100 * 1024, 128, 2}, {1, 200 * 1024, 128, 2}};
+constexpr RingTuning kRingTunings[] = {{5, 25 * 1024, 64, 1}, {2, 100 * 1024, 128, 2}, {1, 200 * 1024, 128, 2}};
 // Eight-lane layout (half the registers a thread): twice the threads a row, so
 // the same rings hold twice the warps.
 constexpr RingTuning kRingTunings8[] = {{4, 50 * 1024, 192, 2}, {2, 100 * 1024, 384, 2}, {1, 200 * 1024, 512, 2}};

@@ -120,6 +120,24 @@ def test_pack_launch_forms(G, k, m, codes):
     parity.check_codes(codes_np(p), Q, v)
 
 
+@pytest.mark.parametrize("k", [4, 64, 256, 768, 1024, 2048, 3072, 4096, 5120, 8192, 12288, 16384, 20480, 24576,
+                               28672])
+@pytest.mark.parametrize("G", [4, 16, 256])
+def test_pack_ring_shapes(G, k):
+    """Every ring shape the launch picks by row length (four-lane layout: five
+    one-stage CTAs per SM, or two or one CTA with two or more stages; eight-lane
+    layout for G <= 16: four, two or one CTA) and the direct form past the rings
+    (k = 28672), on 301 rows."""
+    if k % G:
+        pytest.skip("G must divide k")
+    rng = np.random.default_rng(G * 131 + k)
+    X = special_rows(rng, 301, k)
+    p = gpu_pack(X, G, cr.CODES_BF16)
+    Q, s, v = oracle.pack_rows(X, G)
+    parity.check_scales(p.scale.cpu().numpy(), s)
+    parity.check_codes(codes_np(p), Q, v)
+
+
 def test_pack_hand_worked_rows(golden_dir):
     cases = json.load(open(os.path.join(golden_dir, "hand_worked_rows.json")))["rows"]
     for c in cases:
