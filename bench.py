@@ -153,16 +153,22 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- CPU baseline (the oracle)
-def oracle_sample_run(wl, rows: int, packed_w, X):
+def oracle_sample_run(wl, rows: int, packed_w, X, split=None):
     """One oracle pass over `rows` rows of the workload: for each stage pack,
-    integer GEMM and reconstruct (with the stage's activation)."""
+    integer GEMM and reconstruct (with the stage's activation). `split`, if
+    given, accumulates the seconds spent in the packs and in GEMM + reconstruct."""
     import oracle
 
     H = X[:rows]
     for (Qw, sw, b), st in zip(packed_w, stage_shapes(wl)):
+        t0 = time.perf_counter()
         Qx, sx, _ = oracle.pack_rows(H, wl.G, want_pre_round=False)
+        t1 = time.perf_counter()
         A = oracle.gemm_i32(Qx, Qw, st.k)
         H, _ = oracle.reconstruct(A, sx, sw, b, st.act)
+        if split is not None:
+            split["pack"] += t1 - t0
+            split["gemm"] += time.perf_counter() - t1
 
 
 def cpu_baseline(wl, budget_s: float, steps: int = 1, warmup: int = 0):
@@ -187,17 +193,23 @@ def cpu_baseline(wl, budget_s: float, steps: int = 1, warmup: int = 0):
     for _ in range(warmup):
         oracle_sample_run(wl, rows, packed_w, X)
     times = []
+    split = {"pack": 0.0, "gemm": 0.0}
     for _ in range(steps):
         t0 = time.perf_counter()
-        oracle_sample_run(wl, rows, packed_w, X)
+        oracle_sample_run(wl, rows, packed_w, X, split)
         times.append(time.perf_counter() - t0)
     t = sum(times) / len(times)
     ops = wl.step_ops * rows / wl.m
+    pack_bytes = sum(rows * (5 * st.k + 4) for st in stage_shapes(wl))
     what = " then ".join(f"pack + int GEMM vs {st.n} weight rows + reconstruct" for st in stage_shapes(wl))
+    scope = ("the full shape" if rows == wl.m else
+             f"a {rows}-row subset; rows are independent, so the rate stands for all {wl.m} rows (extrapolated)")
     return {"value": ops / t / 1e12, "unit": "TOPS", "cores": oracle.num_threads(), "kind": "oracle",
             "sample": f"{rows} of {wl.m} rows of {wl.name} ({what}), fp64 oracle, "
-                      f"{len(times)} step(s) of {t:.2f} s",
-            "seconds_per_step": t}
+                      f"{len(times)} step(s) of {t:.2f} s: {scope}",
+            "seconds_per_step": t,
+            "pack_gbs": pack_bytes * steps / max(split["pack"], 1e-9) / 1e9,
+            "gemm_tops": ops * steps / max(split["gemm"], 1e-9) / 1e12}
 
 
 def workload_name(wl) -> str:
@@ -228,7 +240,7 @@ def run_reference(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
         "config": {"workload": workload_name(wl), "sample": cb["sample"]},
-        "cpu_baseline": {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")},
+        "cpu_baseline": {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample", "pack_gbs", "gemm_tops")},
         "e2e": {"value": cb["value"], "unit": "TOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -488,9 +500,13 @@ def run_ours(args):
     pack_avg = kern_ms["pack"]
     pk = peaks()
     gemm_tops = ops / (gemm_avg * 1e-3) / 1e12
-    pack_bytes = sum(wl.m * (4 * st.k + code_b * st.k + 4) for st in stages)
+    # algorithmic bytes of a pack: 4 B read + 1 B code written per element + 4 B scale per row
+    # (the page's I8 codes); the bytes this launch actually stores (bf16 codes: 2 B) beside them
+    pack_bytes = sum(wl.m * (5 * st.k + 4) for st in stages)
+    stored_pack_bytes = sum(wl.m * (4 * st.k + code_b * st.k + 4) for st in stages)
     pack_gbs = pack_bytes / (pack_avg * 1e-3) / 1e9
-    first_pack_bytes = wl.m * (4 * stages[0].k + code_b * stages[0].k + 4)
+    stored_pack_gbs = stored_pack_bytes / (pack_avg * 1e-3) / 1e9
+    first_pack_bytes = wl.m * (5 * stages[0].k + 4)
     first_pack_ms = kern_ms["pack_first"]
     conv_gbs = wl.m * stages[0].k * (4 + code_b) / (conv_ms * 1e-3) / 1e9
     traffic = measured_traffic(wl.name, "i8" if codes == cr.CODES_I8 else "bf16")
@@ -526,7 +542,11 @@ def run_ours(args):
                         if codes == cr.CODES_I8 else {})},
         "roofline_pack": {"bound": "hbm", "achieved": pack_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
                           "frac": pack_gbs / pk["hbm_gbs"], "bytes_per_launch": pack_bytes,
+                          "bytes": "algorithmic: 4 B read + 1 B code per element, 4 B scale per row",
                           "peak_source": f"{pk['source']} copy bandwidth",
+                          "stored": {"bytes_per_launch": stored_pack_bytes, "gbs": stored_pack_gbs,
+                                     "frac": stored_pack_gbs / pk["hbm_gbs"],
+                                     "what": f"the bytes the launch moves with {code_b}-byte codes"},
                           "same_bytes_conversion": {
                               "what": f"torch fp32 -> {str(code_dtype).replace('torch.', '')} copy_ of the "
                                       "same activations, timed like the pack (context, not a step kernel)",
@@ -542,7 +562,8 @@ def run_ours(args):
     }
     if not args.no_cpu_baseline and world == 1:
         cb = cpu_baseline(wl, args.cpu_seconds)
-        line["cpu_baseline"] = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")}
+        line["cpu_baseline"] = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample", "pack_gbs",
+                                                   "gemm_tops")}
     print(json.dumps(line), flush=True)
     if pg:
         pg.destroy_process_group()

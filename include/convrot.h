@@ -250,8 +250,15 @@ convrot_status convrot_linear_lora(const convrot_packed *x, const convrot_packed
  * (CONVROT_NOALLOC_SCRATCH_BYTES = 32 MiB, 256-byte aligned), then
  * convrot_linear_lora reading it. Results equal those of the two calls with
  * a caller's T_ext.
- *   X, ldx, A_ext, lda, k = x->k   as for convrot_lora_down.
+ *   X, ldx  the activations x was packed from: device fp32 [x->rows, ldx],
+ *           ldx >= x->k (k = x->k), 16-byte aligned, ldx % 4 == 0.
+ *   A_ext, lda  convrot_lora_prepare_down's output for this same r:
+ *           device fp32 [2 r, lda], lda >= x->k.
  *   B_ext, lde, r, bias, act, Y, ldy, dev_status   as for convrot_linear_lora.
+ * The library takes the row count of X from x->rows and the rows of A_ext
+ * from r; it cannot see either buffer's size, so an X with fewer rows or
+ * columns, or an A_ext prepared for another rank, makes the kernels read
+ * past those buffers. (The Python binding checks both shapes before the call.)
  * Limits and errors: a request whose T_ext (x->rows * convrot_lora_cols(r)
  * bf16 values; e.g. up to 87381 rows at r = 64, 21845 at r = 256) exceeds
  * the array returns CONVROT_ERR_SCRATCH and launches nothing; a failed

@@ -292,10 +292,38 @@ def convrot_lora_down(X: torch.Tensor, A_ext: torch.Tensor, out: torch.Tensor | 
     return out
 
 
+def _check_matrix(t: torch.Tensor, name: str, dtype, rows: int, min_cols: int, exact_cols: bool = False):
+    """t must be a 2-D row-major `dtype` tensor with `rows` rows and at least (or
+    exactly) `min_cols` columns. The C side receives only a pointer and a leading
+    dimension and cannot check any of this; a tensor that breaks it would make a kernel
+    read outside the buffer. (That it lives on the GPU is checked by _check_cuda.)"""
+    if not isinstance(t, torch.Tensor) or t.dtype != dtype or t.dim() != 2 or t.stride(1) != 1:
+        raise TypeError(f"{name} must be a 2-D row-major {str(dtype).replace('torch.', '')} tensor")
+    if t.shape[0] != rows or (t.shape[1] != min_cols if exact_cols else t.shape[1] < min_cols):
+        want = f"[{rows}, {min_cols}]" if exact_cols else f"[{rows}, >= {min_cols}]"
+        raise ValueError(f"{name} has shape {list(t.shape)}; expected {want}")
+
+
+def _check_cuda(**tensors):
+    for name, t in tensors.items():
+        if not t.is_cuda:
+            raise TypeError(f"{name} must be a CUDA tensor")
+
+
+def _check_lora_up(w: Packed, b_ext: torch.Tensor, r: int):
+    cols = lora_cols(r)
+    if cols == 0:
+        raise ConvrotError(ERR_INVALID_ARG, "lora rank")
+    _check_matrix(b_ext, "B_ext", torch.bfloat16, w.rows, cols)
+
+
 def convrot_linear_lora(x: Packed, w: Packed, bias: torch.Tensor | None, act: int, t_ext: torch.Tensor,
                         b_ext: torch.Tensor, r: int, out: torch.Tensor | None = None,
                         dev_status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """Y = act((Q_x Q_w^T) s_x s_w + b + T_ext B_ext^T): the linear with the LoRA correction."""
+    _check_lora_up(w, b_ext, r)
+    _check_matrix(t_ext, "T_ext", torch.bfloat16, x.rows, lora_cols(r))
+    _check_cuda(T_ext=t_ext, B_ext=b_ext)
     if out is None:
         out = _padded_out(x.rows, w.rows, torch.float32, x.q.device)
     if bias is not None and (bias.dtype != torch.float32 or not bias.is_cuda):
@@ -317,7 +345,16 @@ def convrot_linear_lora_noalloc(x: Packed, w: Packed, bias: torch.Tensor | None,
     library's 32 MiB per-device static array; larger requests raise ERR_SCRATCH. The first
     call on a device looks up that array's address: make it before any stream capture.
     Every call shares the array, so calls that overlap on the GPU race on it. ``out`` is
-    allocated here only when the caller passes none; the C entry point allocates nothing."""
+    allocated here only when the caller passes none; the C entry point allocates nothing.
+
+    X must be the activations x was packed from, [x.rows, x.k] fp32, and A_ext the
+    convrot_lora_prepare_down output for this r ([2 r, >= x.k] fp32); B_ext is
+    [w.rows, >= lora_cols(r)] bf16. These are checked here, before the call, because
+    the C entry point takes their sizes from x, w and r and cannot verify them."""
+    _check_matrix(X, "X", torch.float32, x.rows, x.k, exact_cols=True)
+    _check_matrix(A_ext, "A_ext", torch.float32, 2 * int(r), x.k)
+    _check_lora_up(w, b_ext, r)
+    _check_cuda(X=X, A_ext=A_ext, B_ext=b_ext)
     if out is None:
         out = _padded_out(x.rows, w.rows, torch.float32, x.q.device)
     if bias is not None and (bias.dtype != torch.float32 or not bias.is_cuda):

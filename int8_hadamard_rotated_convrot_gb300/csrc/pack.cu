@@ -1012,9 +1012,13 @@ RingLaunch ring_plan(int k, int lane_bits, const RingTuning (&tunings)[NT])
     return RingLaunch{};
 }
 
+// Launches the ring form; sets *launched = false (and launches nothing) when not
+// one CTA of the planned shape fits on an SM, so that the caller can fall back to
+// a form that needs no resident grid.
 template <typename Kernel>
-cudaError_t launch_ring(Kernel kern, const RingLaunch &L, const PackArgs &a, cudaStream_t stream)
+cudaError_t launch_ring(Kernel kern, const RingLaunch &L, const PackArgs &a, cudaStream_t stream, bool *launched)
 {
+    *launched = false;
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -1028,11 +1032,13 @@ cudaError_t launch_ring(Kernel kern, const RingLaunch &L, const PackArgs &a, cud
     int resident = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident, kern, threads, smem);
     if (e != cudaSuccess) return e;
-    const int per_sm = resident > 0 && resident < L.ctas_per_sm ? resident : L.ctas_per_sm;
+    if (resident <= 0) return cudaSuccess;
+    const int per_sm = resident < L.ctas_per_sm ? resident : L.ctas_per_sm;
     const int64_t nblocks = (a.rows + L.P.rows_per_stage - 1) / L.P.rows_per_stage;
     const int64_t slots = static_cast<int64_t>(sms) * per_sm;
     const int64_t grid = nblocks < slots ? nblocks : slots;
     kern<<<static_cast<unsigned>(grid), threads, smem, stream>>>(a, L.P);
+    *launched = true;
     return cudaGetLastError();
 }
 
@@ -1042,12 +1048,19 @@ cudaError_t launch_g256(const PackArgs &a, cudaStream_t stream)
     const RingLaunch L = ring_plan(a.k, Tile<N>::LB, kRingTunings);
     // the two-phase rotation replaces two shuffle digits for G = 1024 (19.6 -> 18.1 us
     // at K = 3072); for G = 64 and 256, one shuffle digit, it measured no faster
+    bool launched = false;
     if constexpr (N <= 2) {
         const RingLaunch L8 = ring_plan(a.k, 3, kRingTunings8);
-        if (L8.ctas_per_sm > 0) return launch_ring(pack_ring_kernel<N, kBf16, kLanes8>, L8, a, stream);
+        if (L8.ctas_per_sm > 0) {
+            const cudaError_t e = launch_ring(pack_ring_kernel<N, kBf16, kLanes8>, L8, a, stream, &launched);
+            if (e != cudaSuccess || launched) return e;
+        }
     }
-    if (L.ctas_per_sm > 0)
-        return launch_ring(pack_ring_kernel<N, kBf16, N == 5 ? kTwoPhase4 : kLanes4>, L, a, stream);
+    if (L.ctas_per_sm > 0) {
+        const cudaError_t e =
+            launch_ring(pack_ring_kernel<N, kBf16, N == 5 ? kTwoPhase4 : kLanes4>, L, a, stream, &launched);
+        if (e != cudaSuccess || launched) return e;
+    }
     return launch_plan(pack_g256_kernel<N, kBf16>, Shape{Tile<N>::LB, 16}, a, stream);
 }
 

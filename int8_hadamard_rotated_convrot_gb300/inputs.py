@@ -156,7 +156,9 @@ WORKLOADS = {
         Workload("mlp_up", 4096, 3072, 12288, 256, (2, 0)),
         Workload("mlp_down", 4096, 12288, 3072, 256, (2, 1), gelu_input=True),
         Workload("mlp_up_lora", 4096, 3072, 12288, 256, (2, 0), lora_r=64, lora_scale=2.0,
-                 notes="MLP up with a rank-64 runtime LoRA, scale 128/64 (the rank and alpha of the page's example)"),
+                 notes="MLP up with a rank-64 runtime LoRA, scale 128/64 (the rank and lora_alpha of the "
+                       "few-step LoRA in the stable-diffusion-cpp article, section \"A LoRA that loaded "
+                       "320 of its 448 tensors\")"),
         Workload("mlp_pair", 4096, 3072, 12288, 256, (2, 2), act=1, down_n=3072,
                  notes="up projection with GELU fused in its epilogue, then pack + down projection"),
         *[_sweep(G) for G in (4, 16, 64, 256, 1024)],

@@ -1,3 +1,4 @@
+import json
 import os
 import sys
 
@@ -16,3 +17,15 @@ def pytest_configure(config):
 @pytest.fixture(scope="session")
 def golden_dir():
     return os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def pytest_sessionfinish(session, exitstatus):
+    path = os.environ.get("CONVROT_PARITY_RECORD")
+    if not path:
+        return
+    from tests import parity
+
+    if parity.RECORDS:
+        os.makedirs(os.path.dirname(os.path.abspath(path)), exist_ok=True)
+        with open(path, "w") as f:
+            json.dump(parity.RECORDS, f, indent=1)

@@ -343,8 +343,9 @@ def test_linear_end_to_end_tiny(codes):
     parity.check_codes(codes_np(px), ref["Qx"], ref["vx"])
     Qw_ref, _, vw = oracle.pack_rows(W, wl.G)
     parity.check_codes(codes_np(pw), Qw_ref, vw)
-    parity.check_y_end_to_end(Y.cpu().numpy(), ref["Y64"], (codes_np(px), ref["Qx"]), (codes_np(pw), Qw_ref),
-                              px.scale.cpu().numpy(), pw.scale.cpu().numpy())
+    e2e = parity.check_y_end_to_end(Y.cpu().numpy(), ref["Y64"], (codes_np(px), ref["Qx"]),
+                                    (codes_np(pw), Qw_ref), px.scale.cpu().numpy(), pw.scale.cpu().numpy())
+    parity.record(f"tiny ({'i8' if codes == cr.CODES_I8 else 'bf16'} codes)", y_rows=wl.m, **e2e)
     # with the GPU's own codes the integer product and the epilogue are exact
     qx, qw = codes_np(px).astype(np.int8), codes_np(pw).astype(np.int8)
     A_ref = oracle.gemm_i32(qx, qw, wl.k)
@@ -354,8 +355,27 @@ def test_linear_end_to_end_tiny(codes):
     parity.check_y_same_codes(Y.cpu().numpy(), Y64, A_ref, sx, sw, b)
 
 
-FULL = ["attn_qkv", "mlp_up", "mlp_down", "sweep_G4", "sweep_G16", "sweep_G64", "sweep_G1024",
-        "video_n13824"]
+FULL = ["attn_qkv", "mlp_up", "mlp_down", "sweep_G4", "sweep_G16", "sweep_G64", "sweep_G256", "sweep_G1024",
+        "video_n5120", "video_n13824"]
+
+
+def check_pack_all_rows(X, p: cr.Packed, G: int, chunk: int = 4096) -> int:
+    """The pack against the oracle on every row, in chunks of rows: scales and codes.
+    Returns how many codes differ (each one a tie the code rule allows)."""
+    s_all, q_all = p.scale.cpu().numpy(), codes_np(p)
+    flips = 0
+    for r0 in range(0, X.shape[0], chunk):
+        r1 = min(X.shape[0], r0 + chunk)
+        Qc, sc, vc = oracle.pack_rows(X[r0:r1], G)
+        parity.check_scales(s_all[r0:r1], sc)
+        flips += parity.check_codes(q_all[r0:r1], Qc, vc)
+    return flips
+
+
+def sample_rows(m: int, n_rows: int, seed: int = 123) -> np.ndarray:
+    """n_rows seeded random rows plus the last 8 (the ragged tail of the last tile)."""
+    rng = np.random.default_rng(seed)
+    return np.unique(np.concatenate([rng.choice(m - 8, n_rows, replace=False), np.arange(m - 8, m)]))
 
 
 @pytest.mark.slow
@@ -373,19 +393,9 @@ def test_full_size_sampled(name):
     torch.cuda.synchronize()
     assert not torch.isnan(Y).any()
     # the pack on every row, in chunks of rows: scales and codes against the oracle
-    sx_all, qx_all = px.scale.cpu().numpy(), codes_np(px)
-    for r0 in range(0, wl.m, 4096):
-        r1 = min(wl.m, r0 + 4096)
-        Qc, sc, vc = oracle.pack_rows(X[r0:r1], wl.G)
-        parity.check_scales(sx_all[r0:r1], sc)
-        parity.check_codes(qx_all[r0:r1], Qc, vc)
-        del Qc, sc, vc
-    del qx_all
+    pack_flips = check_pack_all_rows(X, px, wl.G)
     # Y on 512 seeded random rows (256 on the largest shape) plus the tail rows
-    rng = np.random.default_rng(123)
-    n_rows = 256 if wl.m * wl.n * wl.k > 2e12 else 512
-    rows = np.unique(np.concatenate([rng.choice(wl.m - 8, n_rows, replace=False),
-                                     np.arange(wl.m - 8, wl.m)]))
+    rows = sample_rows(wl.m, 256 if wl.m * wl.n * wl.k > 2e12 else 512)
     Xs = X[rows]
     Qx_ref, sx_ref, vx = oracle.pack_rows(Xs, wl.G)
     Qw_ref, sw_ref, vw = oracle.pack_rows(W, wl.G)
@@ -396,7 +406,7 @@ def test_full_size_sampled(name):
     sw_gpu = pw.scale.cpu().numpy()
     qw_gpu = codes_np(pw)
     parity.check_scales(sw_gpu, sw_ref)
-    parity.check_codes(qw_gpu, Qw_ref, vw)
+    w_flips = parity.check_codes(qw_gpu, Qw_ref, vw)
     del vw
     Y_rows = Y[torch.from_numpy(rows).cuda()].cpu().numpy()
     # same codes: exact integer product, epilogue within 1e-6
@@ -406,7 +416,9 @@ def test_full_size_sampled(name):
     # end to end against the oracle's own codes
     A_ref = oracle.gemm_i32(Qx_ref, Qw_ref, wl.k)
     _, Y64_ref = oracle.reconstruct(A_ref, sx_ref, sw_ref, b)
-    parity.check_y_end_to_end(Y_rows, Y64_ref, (qx_gpu, Qx_ref), (qw_gpu, Qw_ref), sx_gpu, sw_gpu)
+    e2e = parity.check_y_end_to_end(Y_rows, Y64_ref, (qx_gpu, Qx_ref), (qw_gpu, Qw_ref), sx_gpu, sw_gpu)
+    parity.record(name, qx_codes=int(wl.m * wl.k), qx_flips_all_rows=pack_flips, qw_codes=int(wl.n * wl.k),
+                  qw_flips=w_flips, y_rows=int(rows.size), **e2e)
 
 
 def test_grouped_linears_share_one_pack():
@@ -451,8 +463,134 @@ def test_full_size_attention_grouped_qkv():
     Qw_ref, sw_ref, _ = oracle.pack_rows(np.concatenate(Ws), wl.G, want_pre_round=False)
     A_ref = oracle.gemm_i32(Qx_ref, Qw_ref, wl.k)
     _, Y64 = oracle.reconstruct(A_ref, sx_ref, sw_ref, np.concatenate(bs))
-    parity.check_y_end_to_end(Y[torch.from_numpy(rows).cuda()].cpu().numpy(), Y64, (codes_np(px)[rows], Qx_ref),
-                              (codes_np(pw), Qw_ref), px.scale.cpu().numpy()[rows], pw.scale.cpu().numpy())
+    e2e = parity.check_y_end_to_end(Y[torch.from_numpy(rows).cuda()].cpu().numpy(), Y64,
+                                    (codes_np(px)[rows], Qx_ref), (codes_np(pw), Qw_ref),
+                                    px.scale.cpu().numpy()[rows], pw.scale.cpu().numpy())
+    parity.record("attn_qkv grouped (N = 3 x 3072)", y_rows=int(rows.size), **e2e)
+
+
+@pytest.mark.slow
+def test_full_size_mlp_pair():
+    """The DiT MLP pair as the bench runs it (M4096: K3072 -> N12288 with GELU (erf
+    form) in the up projection's epilogue, pack of that output, -> N3072), into
+    NaN-filled outputs. Stage by stage, each against the oracle given the GPU's own
+    input to that stage: both packs on every row; the hidden activations and the
+    output on 512 seeded rows plus the tail, with the GPU's codes (exact integer
+    product, epilogue within its bound) and end to end from the oracle's codes."""
+    wl = inputs.WORKLOADS["mlp_pair"]
+    G, bf16 = wl.G, cr.CODES_BF16
+    X = inputs.activations(wl)
+    (Wu,), bu = inputs.stage_weights(wl, 0)
+    (Wd,), bd = inputs.stage_weights(wl, 1)
+    px = cr.convrot_pack_activations(to_dev(X), G, bf16)
+    pu = cr.convrot_quantize_weights(to_dev(Wu), G, bf16)
+    pdn = cr.convrot_quantize_weights(to_dev(Wd), G, bf16)
+    H = cr.convrot_linear_act(px, pu, to_dev(bu), wl.act,
+                              out=torch.full((wl.m, wl.n), float("nan"), device="cuda"))
+    ph = cr.convrot_pack_activations(H, G, bf16)
+    Y = cr.convrot_linear(ph, pdn, to_dev(bd), out=torch.full((wl.m, wl.down_n), float("nan"), device="cuda"))
+    torch.cuda.synchronize()
+    assert not torch.isnan(H).any() and not torch.isnan(Y).any()
+    rows = sample_rows(wl.m, 512, seed=321)
+    rows_d = torch.from_numpy(rows).cuda()
+    stats = {"y_rows": int(rows.size)}
+    # stage 1: pack X (every row), up projection + GELU (sampled rows)
+    stats["qx_flips_all_rows"] = check_pack_all_rows(X, px, G)
+    Qu_ref, su_ref, vu = oracle.pack_rows(Wu, G)
+    qu_gpu, su_gpu = codes_np(pu), pu.scale.cpu().numpy()
+    parity.check_scales(su_gpu, su_ref)
+    stats["qw_up_flips"] = parity.check_codes(qu_gpu, Qu_ref, vu)
+    del vu
+    qx_rows, sx_rows = codes_np(px)[rows], px.scale.cpu().numpy()[rows]
+    H_rows = H[rows_d].cpu().numpy()
+    A1 = oracle.gemm_i32(qx_rows.astype(np.int8), qu_gpu.astype(np.int8), wl.k)
+    _, H64 = oracle.reconstruct(A1, sx_rows, su_gpu, bu, wl.act)
+    parity.check_y_act_same_codes(H_rows, H64, A1, sx_rows, su_gpu, bu)
+    Qx_ref, sx_ref, _ = oracle.pack_rows(X[rows], G, want_pre_round=False)
+    A1_ref = oracle.gemm_i32(Qx_ref, Qu_ref, wl.k)
+    H_chain, H64_ref = oracle.reconstruct(A1_ref, sx_ref, su_ref, bu, wl.act)  # H_chain: fp32, as stored
+    e1 = parity.check_y_end_to_end(H_rows, H64_ref, (qx_rows, Qx_ref), (qu_gpu, Qu_ref), sx_rows, su_gpu)
+    parity.record("mlp_pair up + GELU (stage 1)", **stats, **e1)
+    del A1, H64, A1_ref, H64_ref
+    # stage 2: the pack of the GPU's hidden activations, every row
+    H_np = H.cpu().numpy()
+    ph_flips = check_pack_all_rows(H_np, ph, G, chunk=1024)
+    # stage 3: down projection from the GPU's hidden activations (sampled rows)
+    Qd_ref, sd_ref, vd = oracle.pack_rows(Wd, G)
+    qd_gpu, sd_gpu = codes_np(pdn), pdn.scale.cpu().numpy()
+    parity.check_scales(sd_gpu, sd_ref)
+    qd_flips = parity.check_codes(qd_gpu, Qd_ref, vd)
+    del vd
+    qh_rows, sh_rows = codes_np(ph)[rows], ph.scale.cpu().numpy()[rows]
+    Y_rows = Y[rows_d].cpu().numpy()
+    A2 = oracle.gemm_i32(qh_rows.astype(np.int8), qd_gpu.astype(np.int8), wl.n)
+    _, Y64 = oracle.reconstruct(A2, sh_rows, sd_gpu, bd)
+    parity.check_y_same_codes(Y_rows, Y64, A2, sh_rows, sd_gpu, bd)
+    Qh_ref, sh_ref, _ = oracle.pack_rows(H_np[rows], G, want_pre_round=False)
+    A2_ref = oracle.gemm_i32(Qh_ref, Qd_ref, wl.n)
+    _, Y64_ref = oracle.reconstruct(A2_ref, sh_ref, sd_ref, bd)
+    e3 = parity.check_y_end_to_end(Y_rows, Y64_ref, (qh_rows, Qh_ref), (qd_gpu, Qd_ref), sh_rows, sd_gpu)
+    # the whole chain in the oracle alone (its own hidden activations, rounded to fp32
+    # as they are stored), against the GPU's output: recorded, not a tolerance rule
+    Qc, sc, _ = oracle.pack_rows(H_chain, G, want_pre_round=False)
+    _, Y64_chain = oracle.reconstruct(oracle.gemm_i32(Qc, Qd_ref, wl.n), sc, sd_ref, bd)
+    chain = float(np.max(np.abs(Y_rows - Y64_chain)) / (1e-3 * np.max(np.abs(Y64_chain))))
+    parity.record("mlp_pair down (stage 3, from the GPU's hidden activations)", y_rows=int(rows.size),
+                  qh_flips_all_rows=ph_flips, qw_down_flips=qd_flips,
+                  chain_max_err_over_plain=chain, **e3)
+
+
+@pytest.mark.slow
+def test_full_size_mlp_up_lora():
+    """MLP up with the rank-64 runtime LoRA (scale 2) as the bench runs it: LoRA down
+    from the unrotated X, pack, and the linear with the correction chunk, into
+    NaN-filled outputs. The pack on every row; T and Y on 512 seeded rows plus the
+    tail: T against the fp64 oracle within its split-TF32 bound, Y with the GPU's
+    codes within the base-plus-correction bound, and end to end from the oracle's
+    codes and correction."""
+    wl = inputs.WORKLOADS["mlp_up_lora"]
+    G, r, bf16 = wl.G, wl.lora_r, cr.CODES_BF16
+    X = inputs.activations(wl)
+    (W,), b = inputs.stage_weights(wl, 0)
+    Al, Bl = inputs.lora_weights(wl)
+    Xd = to_dev(X)
+    A_ext = cr.convrot_lora_prepare_down(to_dev(Al))
+    B_ext = cr.convrot_lora_prepare(to_dev(Bl), wl.lora_scale)
+    pw = cr.convrot_quantize_weights(to_dev(W), G, bf16)
+    T_ext = cr.convrot_lora_down(Xd, A_ext)
+    px = cr.convrot_pack_activations(Xd, G, bf16)
+    Y = cr.convrot_linear_lora(px, pw, to_dev(b), wl.act, T_ext, B_ext, r,
+                               out=torch.full((wl.m, wl.n), float("nan"), device="cuda"))
+    torch.cuda.synchronize()
+    assert not torch.isnan(Y).any()
+    flips = check_pack_all_rows(X, px, G)
+    rows = sample_rows(wl.m, 512, seed=654)
+    rows_d = torch.from_numpy(rows).cuda()
+    Xs = X[rows]
+    # T on the sampled rows
+    t = T_ext[rows_d].float().cpu().numpy()
+    T_ref, D = oracle.lora_delta(Xs, Al, Bl, wl.lora_scale)
+    l1_t = np.abs(Xs.astype(np.float64)) @ np.abs(Al.astype(np.float64)).T
+    parity.check_lora_t(t[:, :r].astype(np.float64) + t[:, 2 * r:3 * r], T_ref, l1_t, wl.k)
+    # Y with the GPU's codes: exact integer product, correction within its bound
+    Qw_ref, sw_ref, vw = oracle.pack_rows(W, G)
+    qw_gpu, sw_gpu = codes_np(pw), pw.scale.cpu().numpy()
+    parity.check_scales(sw_gpu, sw_ref)
+    w_flips = parity.check_codes(qw_gpu, Qw_ref, vw)
+    del vw
+    qx_rows, sx_rows = codes_np(px)[rows], px.scale.cpu().numpy()[rows]
+    Y_rows = Y[rows_d].cpu().numpy()
+    A = oracle.gemm_i32(qx_rows.astype(np.int8), qw_gpu.astype(np.int8), wl.k)
+    _, Y64 = oracle.reconstruct(A, sx_rows, sw_gpu, b, wl.act, add=D)
+    l1 = wl.lora_scale * l1_t @ np.abs(Bl.astype(np.float64)).T
+    parity.check_y_lora_same_codes(Y_rows, Y64, A, sx_rows, sw_gpu, b, l1, wl.k, r, wl.act)
+    assert np.abs(D).mean() > 0.05 * np.abs(Y64).mean()  # the correction is not negligible
+    # end to end from the oracle's codes and correction
+    Qx_ref, sx_ref, _ = oracle.pack_rows(Xs, G, want_pre_round=False)
+    _, Y64_ref = oracle.reconstruct(oracle.gemm_i32(Qx_ref, Qw_ref, wl.k), sx_ref, sw_ref, b, wl.act, add=D)
+    e2e = parity.check_y_end_to_end(Y_rows, Y64_ref, (qx_rows, Qx_ref), (qw_gpu, Qw_ref), sx_rows, sw_gpu)
+    parity.record("mlp_up_lora (r 64, scale 2)", y_rows=int(rows.size), qx_flips_all_rows=flips, qw_flips=w_flips,
+                  **e2e)
 
 
 def test_graph_replay_equals_eager_steps():

@@ -65,6 +65,43 @@ def test_noalloc_checks_the_linear_before_any_device_work():
     assert lib.convrot_linear_lora_noalloc(*args(x, w_other_g, 8, FAKE)) == cr.ERR_GROUP_SIZE
 
 
+def test_noalloc_wrapper_rejects_tensors_the_c_side_cannot_check():
+    """The C entry point takes X's and A_ext's sizes from x and r, so the binding
+    checks the tensors before the call: wrong dtype, layout, shape or device
+    raise here, on the host, and nothing reaches the library."""
+    cbuild.build()
+    cr.load()
+    m, k, n, r = 8, 256, 16, 64
+    cols = cr.lora_cols(r)
+    x = cr.Packed(torch.zeros((m, cr.convrot_ldq(k)), dtype=torch.bfloat16), torch.zeros(m), m, k, 256,
+                  cr.CODES_BF16)
+    w = cr.Packed(torch.zeros((n, cr.convrot_ldq(k)), dtype=torch.bfloat16), torch.zeros(n), n, k, 256,
+                  cr.CODES_BF16)
+    X = torch.zeros((m, k))
+    A_ext = torch.zeros((2 * r, k))
+    B_ext = torch.zeros((n, cols), dtype=torch.bfloat16)
+    call = lambda X=X, A=A_ext, B=B_ext: cr.convrot_linear_lora_noalloc(x, w, None, 0, X, A, B, r,
+                                                                         out=torch.zeros((m, n)))
+    with pytest.raises(TypeError):
+        call(X=X.double())                        # not fp32
+    with pytest.raises(TypeError):
+        call(X=torch.zeros((k, m)).t())           # not row-major
+    with pytest.raises(ValueError):
+        call(X=X[: m - 1])                        # fewer rows than x was packed from
+    with pytest.raises(ValueError):
+        call(X=torch.zeros((m, k - 4)))           # fewer columns than x.k
+    with pytest.raises(ValueError):
+        call(A=torch.zeros((2 * 32, k)))          # prepared for another rank
+    with pytest.raises(ValueError):
+        call(A=torch.zeros((2 * r, k - 4)))       # narrower than x.k
+    with pytest.raises(TypeError):
+        call(B=B_ext.float())                     # B_ext is bf16
+    with pytest.raises(ValueError):
+        call(B=B_ext[:, : cols - 8])              # fewer columns than lora_cols(r)
+    with pytest.raises(TypeError, match="CUDA"):
+        call()                                    # right shapes, but host tensors
+
+
 def _case(rng, m, n, k, r):
     X = rng.standard_normal((m, k)).astype(np.float32)
     W = (0.02 * rng.standard_normal((n, k))).astype(np.float32)
