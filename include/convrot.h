@@ -61,7 +61,9 @@ typedef enum {
 
 /* Element type of the stored codes. Both hold the same integers in
  * [-127, 127]; BF16 represents every one of them exactly and is the operand
- * type the tensor-core GEMM reads directly. */
+ * type the tensor-core GEMM reads directly. I8 (the page's storage) is read
+ * by the same tensor-core GEMM, which widens it to f16 in shared memory
+ * (m <= 128: a warp-level int8 MMA kernel); both give the same integers. */
 typedef enum {
     CONVROT_CODES_I8 = 0,
     CONVROT_CODES_BF16 = 1

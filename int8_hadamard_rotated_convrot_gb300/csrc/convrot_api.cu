@@ -232,8 +232,8 @@ convrot_status run_gemm(const convrot_packed *x, const convrot_packed *w, const 
     g.lora_ldt = lora.ldt;
     g.lora_b = lora.b;
     g.lora_ldb = lora.ldb;
-    cudaError_t e = x->codes == CONVROT_CODES_I8 ? convrot::launch_gemm_imma(g, stream)
-                                                 : convrot::launch_gemm_tc(g, stream);
+    g.i8 = x->codes == CONVROT_CODES_I8 ? 1 : 0;
+    cudaError_t e = convrot::launch_gemm_tc(g, stream);
     if (e == cudaErrorNotSupported) return CONVROT_ERR_UNSUPPORTED;
     return e == cudaSuccess ? CONVROT_OK : CONVROT_ERR_CUDA;
 }

@@ -521,7 +521,17 @@ struct Cfg {
     // kind::f16: D fp32, A and B bf16, K-major, M = 256 (both CTAs), N = BN
     static constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(BN >> 3) << 17) |
                                        (uint32_t(256 >> 4) << 24);
+    // I8 codes: the TMA brings 64-wide K slices of int8 rows into a raw ring
+    // (8 KB of A and 8 KB of B a stage), and the converter warps widen them to
+    // f16 in the usual 32 KB stages, which the MMA reads as kind::f16 with f16
+    // operands (A and B of one type; every integer in [-127, 127] is exact).
+    static constexpr int RAW_A = BMC * BK, RAW_B = BNC * BK, RAW_STAGE = RAW_A + RAW_B;
+    static constexpr int STAGES_I8 = 5, RAW_STAGES = 2;
+    static constexpr int SMEM_BYTES_I8 =
+        1024 + STAGES_I8 * STAGE_BYTES + RAW_STAGES * RAW_STAGE + PAIR_OUT_BYTES + BAR_BYTES;
+    static constexpr uint32_t kIdescF16 = (1u << 4) | (uint32_t(BN >> 3) << 17) | (uint32_t(256 >> 4) << 24);
     static_assert(STAGE_BYTES % 1024 == 0, "stages stay 1024-byte aligned for the 128-byte swizzle");
+    static_assert(SMEM_BYTES_I8 <= 232448, "I8 rings fit the shared memory of one CTA");
 };
 
 __device__ __forceinline__ uint32_t cluster_rank()
@@ -565,6 +575,88 @@ __device__ __forceinline__ void mma_pair(uint32_t d_tmem, uint64_t a, uint64_t b
         : "memory");
 }
 
+// Bounded wait with acquire at cluster scope: the phase completes by arrivals
+// (release, cluster scope) of threads in either CTA of the pair.
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity)
+{
+    auto try_once = [&]() {
+        uint32_t ok;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        return ok != 0;
+    };
+    if (try_once()) return true;
+    const uint64_t t0 = globaltimer();
+    for (;;) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (try_once()) return true;
+        if (globaltimer() - t0 > kTimeoutNs) return false;
+    }
+}
+
+// 16 int8 codes (one 16-byte chunk of a raw row) to 16 f16 values in two
+// 16-byte chunks. Per 32-bit word: flip the sign bits (byte b + 128, in
+// [1, 255]), place each byte in the low mantissa byte of the f16 1024.0
+// (0x64nn = 1024 + b + 128), and subtract 1152 = 1024 + 128: exact, since every
+// value involved is an integer below 2048.
+__device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t &lo, uint32_t &hi)
+{
+    const uint32_t u = w ^ 0x80808080u;
+    const uint32_t a = __byte_perm(u, 0x64646464u, 0x4140), b = __byte_perm(u, 0x64646464u, 0x4342);
+    asm("add.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(0xE480E480u));
+    asm("add.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(0xE480E480u));
+}
+
+// Widens rows [0, rows) of a raw int8 tile (64 bytes a row, unswizzled, as the
+// TMA wrote it) into a K-major f16 tile in the 128-byte swizzle the MMA reads
+// (16-byte chunk c of row r at c ^ (r & 7)). Thread t of the nt converter
+// threads takes raw chunks t, t + nt, ...: eight consecutive threads read 128
+// contiguous bytes and write eight distinct chunks of two rows, so neither side
+// has bank conflicts.
+// Chunks go in batches of eight a thread, all eight loads issued before any
+// conversion, so that the shared-memory latency overlaps.
+__device__ __forceinline__ void widen_rows(uint32_t src, uint32_t dst, int rows, int t, int nt)
+{
+    constexpr int kBatch = 4;
+    const int n = rows * 4;
+#pragma unroll 1
+    for (int i0 = t; i0 < n; i0 += kBatch * nt) {
+        uint32_t w[kBatch][4];
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+            const int i = i0 + j * nt;
+            if (i < n)
+                asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                             : "=r"(w[j][0]), "=r"(w[j][1]), "=r"(w[j][2]), "=r"(w[j][3])
+                             : "r"(src + static_cast<uint32_t>(i) * 16u));
+        }
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+            const int i = i0 + j * nt;
+            if (i >= n) break;
+            const int r = i >> 2, c = i & 3;
+            uint32_t h[8];
+            i8x4_to_f16x4(w[j][0], h[0], h[1]);
+            i8x4_to_f16x4(w[j][1], h[2], h[3]);
+            i8x4_to_f16x4(w[j][2], h[4], h[5]);
+            i8x4_to_f16x4(w[j][3], h[6], h[7]);
+            const uint32_t row = dst + static_cast<uint32_t>(r) * 128u, x = static_cast<uint32_t>(r & 7);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row + (((2u * c) ^ x) << 4)), "r"(h[0]),
+                         "r"(h[1]), "r"(h[2]), "r"(h[3])
+                         : "memory");
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row + (((2u * c + 1u) ^ x) << 4)),
+                         "r"(h[4]), "r"(h[5]), "r"(h[6]), "r"(h[7])
+                         : "memory");
+        }
+    }
+}
+
 // Arrive (once the issuing thread's MMAs complete) on the barrier at this offset in both CTAs.
 __device__ __forceinline__ void commit_both(uint32_t bar)
 {
@@ -599,33 +691,56 @@ constexpr int PAIR_THREADS = 128 + PAIR_EPI_WARPS * 32;
 constexpr int PAIR_COLS = 64;  // columns per epilogue warp
 constexpr int kRegsWg0 = 40, kRegsEpi = 104;
 static_assert(4 * 32 * kRegsWg0 + PAIR_EPI_WARPS * 32 * kRegsEpi <= PAIR_THREADS * 96, "register split");
+// With int8 operands a second warpgroup of converter warps joins (warps 4-7,
+// beside warps 2 and 3 of warpgroup 0): 768 threads, launched at 80 registers
+// a thread; warpgroups 0 and 1 keep 48 and the epilogue takes 96:
+// 2 x 128 x 48 + 16 x 32 x 96 = 61440 = 768 x 80.
+constexpr int PAIR_THREADS_I8 = 256 + PAIR_EPI_WARPS * 32;
+constexpr int kRegsConvI8 = 48, kRegsEpiI8 = 96;
+static_assert(2 * 128 * kRegsConvI8 + PAIR_EPI_WARPS * 32 * kRegsEpiI8 <= PAIR_THREADS_I8 * 80, "register split (I8)");
 static_assert(PAIR_EPI_WARPS * PAIR_NBUF * PAIR_BUF_BYTES == PAIR_OUT_BYTES, "staging per epilogue warp");
 
 // kLora: after each tile's K slices, the producer streams lora_kst more slices
 // from tmLa (T_ext rows) and tmLb (B_ext rows); the MMA runs them as one extra
 // chunk whose fp32 sums are not promoted to int32 but added to the output.
-template <int BN, bool kRawInt32, int kAct, bool kLora>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
+// kI8: the operands are int8 codes. The producer loads them into the raw ring
+// (tmA, tmB, tmBt are int8 maps, unswizzled), warps 2 and 3 of each CTA widen
+// each raw stage into an f16 stage and arrive on the even CTA's full barrier,
+// and the MMA runs kind::f16 on f16 operands.
+constexpr int kConvWarps = 6;
+
+template <int BN, bool kRawInt32, int kAct, bool kLora, bool kI8 = false>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kI8 ? PAIR_THREADS_I8 : PAIR_THREADS, 1)
     gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmLa,
                         const __grid_constant__ CUtensorMap tmLb, const __grid_constant__ CUtensorMap tmBt,
                         const __grid_constant__ CUtensorMap tmLbt, TcParams p)
 {
     using C = Cfg<BN>;
-    constexpr int STAGES = C::STAGES, STAGE_BYTES = C::STAGE_BYTES, A_BYTES = C::A_BYTES, BNP = C::BNP, BNC = C::BNC;
+    static_assert(!(kI8 && kLora), "the LoRA chunk is bf16: it runs with bf16 codes only");
+    constexpr int STAGES = kI8 ? C::STAGES_I8 : C::STAGES, RSTAGES = kI8 ? C::RAW_STAGES : 0;
+    constexpr int STAGE_BYTES = C::STAGE_BYTES, A_BYTES = C::A_BYTES, BNP = C::BNP, BNC = C::BNC;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = static_cast<uint32_t>(__cvta_generic_to_shared(smem_raw));
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *gbase = smem_raw + (base - raw);
-    const uint32_t out_base = base + STAGES * STAGE_BYTES;
+    const uint32_t raw_base = base + STAGES * STAGE_BYTES;  // kI8: the int8 ring
+    const uint32_t out_base = raw_base + RSTAGES * C::RAW_STAGE;
     const uint32_t bars = out_base + PAIR_OUT_BYTES;
     auto full_bar = [&](int s) { return bars + 8u * s; };
     auto empty_bar = [&](int s) { return bars + 8u * (STAGES + s); };
     auto accf_bar = [&](int b) { return bars + 8u * (2 * STAGES + b); };
     auto acce_bar = [&](int b) { return bars + 8u * (2 * STAGES + 2 + b); };
     const uint32_t done_bar = bars + 8u * (2 * STAGES + 4);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + STAGES * STAGE_BYTES + PAIR_OUT_BYTES + 160);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + STAGES * STAGE_BYTES + PAIR_OUT_BYTES + 164);
+    auto raw_full = [&](int r) { return bars + 8u * (2 * STAGES + 5 + r); };
+    auto raw_empty = [&](int r) { return bars + 8u * (2 * STAGES + 5 + RSTAGES + r); };
+    // kI8, odd CTA: its converter warps arrive here; one thread forwards each phase to the even CTA
+    auto conv_done = [&](int s) { return bars + 8u * (2 * STAGES + 5 + 2 * RSTAGES + s); };
+    constexpr int kSlotOff = kI8 ? 8 * (3 * STAGES + 5 + 2 * RSTAGES) + 8 : 160;
+    static_assert(kSlotOff + 8 <= BAR_BYTES, "barriers, TMEM slot and abort flag fit their region");
+    uint8_t *const slots = gbase + (out_base - base) + PAIR_OUT_BYTES + kSlotOff;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(slots);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(slots + 4);
 
     const uint32_t rank = cluster_rank();
     const bool leader = rank == 0;
@@ -639,8 +754,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(full_bar(s), 1);
+            // kI8: a converted stage is complete when the even CTA's converter warps and the
+            // odd CTA's forwarding thread arrived
+            mbar_init(full_bar(s), kI8 ? kConvWarps + 1 : 1);
             mbar_init(empty_bar(s), 1);
+            if constexpr (kI8) mbar_init(conv_done(s), kConvWarps);
+        }
+        for (int r = 0; r < RSTAGES; ++r) {
+            mbar_init(raw_full(r), 1);
+            mbar_init(raw_empty(r), kConvWarps);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(accf_bar(b), 1);
@@ -674,9 +796,56 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
         if (p.dev_status) atomicExch(p.dev_status, static_cast<int32_t>(CONVROT_ERR_TIMEOUT));
     };
 
+    // kI8: converter thread ct of kConvWarps * 32 widens each raw int8 stage of
+    // this CTA into the next f16 stage, then the stage is released to the
+    // producer and announced to the even CTA's MMA thread
+    auto run_converter = [&](int ct) {
+        int rs = 0, stage = 0;
+        uint32_t rph = 0, phase = 0;
+        bool ok = true;
+        auto convert = [&](int b_rows) {
+            for (int ks = 0; ks < kst; ++ks) {
+                // every lane waits; the warp goes on only if all of them saw both phases
+                const bool got = !*abort_flag && mbar_wait(raw_full(rs), rph) && mbar_wait(empty_bar(stage), phase ^ 1u);
+                if (!__all_sync(0xffffffffu, got)) {
+                    ok = false;
+                    return;
+                }
+                const uint32_t ra = raw_base + rs * C::RAW_STAGE, sa = base + stage * STAGE_BYTES;
+                widen_rows(ra, sa, BMC, ct, kConvWarps * 32);
+                widen_rows(ra + C::RAW_A, sa + A_BYTES, b_rows, ct, kConvWarps * 32);
+                // the generic-proxy writes are made visible to the tensor cores' reads
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(raw_empty(rs));
+                    // a local arrive; a release at cluster scope from every converter warp
+                    // stalled each of them ~900 cycles a stage
+                    mbar_arrive(leader ? full_bar(stage) : conv_done(stage));
+                }
+                if (++rs == RSTAGES) {
+                    rs = 0;
+                    rph ^= 1u;
+                }
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        };
+        for (int64_t t = pair_id; t < p.full_tiles && ok; t += n_pairs) convert(BNC);
+        {
+            const int sp = p.tail_split, wd = BNP / sp;
+            const int64_t n_items = (n_tiles - p.full_tiles) * sp;
+            for (int64_t u = pair_id; u < n_items && ok; u += n_pairs) convert(wd / 2);
+        }
+        if (!ok) fail();
+    };
+    constexpr int kEpi0 = kI8 ? 8 : 4;  // first epilogue warp
+
     if (warp < 4) {
       // warpgroup 0: every warp runs this one instruction, then the roles split
-      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsWg0));
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kI8 ? kRegsConvI8 : kRegsWg0));
       if (warp == 0) {
         if (lane == 0) {
             int stage = 0;
@@ -705,11 +874,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
                     }
                 }
             };
+            // kI8: every K slice into this CTA's raw ring, completion on its own barrier
+            int rs = 0;
+            uint32_t rph = 0;
+            auto produce8 = [&](int mt, int brow, uint32_t tx, const CUtensorMap *bmap) {
+                const int arow = mt * 2 * BMC + static_cast<int>(rank) * BMC;
+                for (int ks = 0; ks < kst; ++ks) {
+                    if (*abort_flag || !mbar_wait(raw_empty(rs), rph ^ 1u)) {
+                        ok = false;
+                        return;
+                    }
+                    const uint32_t ra = raw_base + rs * C::RAW_STAGE;
+                    mbar_arrive_expect_tx(raw_full(rs), tx);
+                    tma_load_2d(ra, &tmA, ks * BK, arow, raw_full(rs));
+                    tma_load_2d(ra + C::RAW_A, bmap, ks * BK, brow, raw_full(rs));
+                    ++issued;
+                    if (++rs == RSTAGES) {
+                        rs = 0;
+                        rph ^= 1u;
+                    }
+                }
+            };
             for (int64_t t = pair_id; t < p.full_tiles && ok; t += n_pairs) {
                 int64_t mt64, nt64;
                 tile_coords(t, n_mt, n_nt, mt64, nt64);
-                produce(static_cast<int>(mt64), static_cast<int>(nt64) * BNP + static_cast<int>(rank) * BNC,
-                        2u * STAGE_BYTES, &tmB, &tmLb);
+                const int brow = static_cast<int>(nt64) * BNP + static_cast<int>(rank) * BNC;
+                if constexpr (kI8)
+                    produce8(static_cast<int>(mt64), brow, C::RAW_STAGE, &tmB);
+                else
+                    produce(static_cast<int>(mt64), brow, 2u * STAGE_BYTES, &tmB, &tmLb);
             }
             {  // the last, partial wave: its tiles split along N into items
                 const int sp = p.tail_split, wd = BNP / sp;
@@ -719,11 +912,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
                     tile_coords(p.full_tiles + u / sp, n_mt, n_nt, mt64, nt64);
                     const int brow = static_cast<int>(nt64) * BNP + static_cast<int>(u % sp) * wd +
                                      static_cast<int>(rank) * (wd / 2);
-                    produce(static_cast<int>(mt64), brow, 2u * static_cast<uint32_t>(A_BYTES + (wd / 2) * BK * 2),
-                            sp > 1 ? &tmBt : &tmB, sp > 1 ? &tmLbt : &tmLb);
+                    if constexpr (kI8)
+                        produce8(static_cast<int>(mt64), brow, static_cast<uint32_t>(C::RAW_A + (wd / 2) * BK),
+                                 sp > 1 ? &tmBt : &tmB);
+                    else
+                        produce(static_cast<int>(mt64), brow, 2u * static_cast<uint32_t>(A_BYTES + (wd / 2) * BK * 2),
+                                sp > 1 ? &tmBt : &tmB, sp > 1 ? &tmLbt : &tmLb);
                 }
             }
-            if (!ok) {
+            if (!ok && kI8) {
+                fail();
+                // this CTA's copies in flight land before its shared memory goes away
+                for (int i = 0; i < RSTAGES && i < issued; ++i) {
+                    if (--rs < 0) {
+                        rs = RSTAGES - 1;
+                        rph ^= 1u;
+                    }
+                    mbar_wait(raw_full(rs), rph);
+                }
+            } else if (!ok) {
                 fail();
                 if (leader) {
                     // both CTAs' copies for the stages armed here land before shared memory goes away
@@ -758,7 +965,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
                     const int ks0 = c < n_chunks ? c * CHUNK_KSTAGES : kst;
                     const int ks1 = c < n_chunks ? (ks0 + CHUNK_KSTAGES < kst ? ks0 + CHUNK_KSTAGES : kst) : kst + lkst;
                     for (int ks = ks0; ks < ks1; ++ks) {
-                        if (*abort_flag || !mbar_wait(full_bar(stage), phase)) {
+                        const bool got = kI8 ? mbar_wait_cluster(full_bar(stage), phase) : mbar_wait(full_bar(stage), phase);
+                        if (*abort_flag || !got) {
                             ok = false;
                             return;
                         }
@@ -777,25 +985,67 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
                     commit_both(accf_bar(buf));
                 }
             };
-            for (int64_t t = pair_id; t < p.full_tiles && ok; t += n_pairs) mma_tile(C::kIdesc);
+            constexpr uint32_t kId = kI8 ? C::kIdescF16 : C::kIdesc;
+            for (int64_t t = pair_id; t < p.full_tiles && ok; t += n_pairs) mma_tile(kId);
             {
                 const int sp = p.tail_split;
                 const int64_t n_items = (n_tiles - p.full_tiles) * sp;
-                const uint32_t idesc = (C::kIdesc & ~(0x3Fu << 17)) | (static_cast<uint32_t>((BNP / sp) >> 3) << 17);
+                const uint32_t idesc = (kId & ~(0x3Fu << 17)) | (static_cast<uint32_t>((BNP / sp) >> 3) << 17);
                 for (int64_t u = pair_id; u < n_items && ok; u += n_pairs) mma_tile(idesc);
             }
             if (!ok) fail();
             commit_local(done_bar);
             mbar_wait(done_bar, 0);
+        } else if (kI8 && !leader && lane == 0) {
+            // odd CTA: forward converted stages to the even CTA's full barriers. A fence at
+            // cluster scope orders the converter warps' writes (acquired from conv_done)
+            // before relaxed arrivals; it costs ~1200 cycles however little this thread
+            // wrote, so one fence covers every stage already converted when it runs.
+            int64_t n_stages = 0;
+            for (int64_t t = pair_id; t < p.full_tiles; t += n_pairs) n_stages += kst;
+            for (int64_t u = pair_id; u < (n_tiles - p.full_tiles) * p.tail_split; u += n_pairs) n_stages += kst;
+            int stage = 0;
+            uint32_t phase = 0;
+            for (int64_t i = 0; i < n_stages;) {
+                if (*abort_flag || !mbar_wait(conv_done(stage), phase)) {
+                    fail();
+                    break;
+                }
+                int n = 1, s1 = stage;
+                uint32_t ph1 = phase;
+                for (;;) {  // the stages after it that are already converted
+                    if (++s1 == STAGES) {
+                        s1 = 0;
+                        ph1 ^= 1u;
+                    }
+                    if (n == STAGES - 1 || i + n >= n_stages || !mbar_try_wait(conv_done(s1), ph1)) break;
+                    ++n;
+                }
+                asm volatile("fence.acq_rel.cluster;" ::: "memory");
+                for (int j = 0; j < n; ++j, ++i) {
+                    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(
+                                     map_to_rank(full_bar(stage), 0))
+                                 : "memory");
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
         }
         __syncwarp();
+      } else if (kI8) {
+        run_converter((warp - 2) * 32 + lane);  // warps 2 and 3
       }
+    } else if (kI8 && warp < 8) {
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsConvI8));
+      run_converter((warp - 2) * 32 + lane);  // warps 4-7
     } else {
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsEpi));
-        const int q = warp & 3;            // TMEM lane quadrant (warp % 4)
-        const int part = (warp - 4) >> 2;  // 64-column slice of the tile or item
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kI8 ? kRegsEpiI8 : kRegsEpi));
+        const int q = warp & 3;                 // TMEM lane quadrant (warp % 4)
+        const int part = (warp - kEpi0) >> 2;  // 64-column slice of the tile or item
         const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
-        const uint32_t out_smem = out_base + (warp - 4) * PAIR_NBUF * PAIR_BUF_BYTES;
+        const uint32_t out_smem = out_base + (warp - kEpi0) * PAIR_NBUF * PAIR_BUF_BYTES;
         uint32_t store_iter = 0;
         uint32_t chunk_iter = 0;
         bool ok = true;
@@ -934,6 +1184,21 @@ bool make_map(CUtensorMap *map, const void *base, int64_t rows, int64_t kpad, in
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D map over a [rows, ld] int8 matrix, box = box_rows x 64 elements, unswizzled
+// (the converter warps read it row by row and write the swizzled f16 stage).
+bool make_map8(CUtensorMap *map, const void *base, int64_t rows, int64_t kpad, int64_t ld, uint32_t box_rows)
+{
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(kpad), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 2-D map over the [m, ld] output (fp32 Y or int32 A): 32 rows x box_cols boxes,
 // 128-byte swizzle for 32 columns, 64-byte swizzle for 16.
 bool make_out_map(CUtensorMap *map, void *base, int64_t m, int64_t n, int64_t ld, bool int32_out, int box_cols = OUT_BOX)
@@ -958,7 +1223,10 @@ cudaError_t launch_pair(const GemmArgs &g, TcParams p, int sms, cudaStream_t str
     if (!make_out_map(&ty, g.a ? static_cast<void *>(g.a) : static_cast<void *>(g.y), g.m, g.n, g.ldy, g.a != nullptr,
                       pair::PAIR_BW))
         return cudaErrorInvalidValue;
-    if (!make_map(&pa, g.qx, g.m, g.kpad, g.ldqx, pair::BMC) || !make_map(&pb, g.qw, g.n, g.kpad, g.ldqw, C::BNC))
+    auto operand_map = [&](CUtensorMap *m, const void *q, int64_t rows, int64_t ld, uint32_t box_rows) {
+        return g.i8 ? make_map8(m, q, rows, g.kpad, ld, box_rows) : make_map(m, q, rows, g.kpad, ld, box_rows);
+    };
+    if (!operand_map(&pa, g.qx, g.m, g.ldqx, pair::BMC) || !operand_map(&pb, g.qw, g.n, g.ldqw, C::BNC))
         return cudaErrorInvalidValue;
     la = pa;
     lb = pb;
@@ -984,16 +1252,25 @@ cudaError_t launch_pair(const GemmArgs &g, TcParams p, int sms, cudaStream_t str
     CUtensorMap pbt = pb, lbt = lb;
     if (split > 1) {
         const uint32_t rows = static_cast<uint32_t>(C::BNC / split);
-        if (!make_map(&pbt, g.qw, g.n, g.kpad, g.ldqw, rows)) return cudaErrorInvalidValue;
+        if (!operand_map(&pbt, g.qw, g.n, g.ldqw, rows)) return cudaErrorInvalidValue;
         if (g.lora_r > 0 && !make_map(&lbt, g.lora_b, g.n, lora_cols(g.lora_r), g.lora_ldb, rows))
             return cudaErrorInvalidValue;
     }
+    const int smem = g.i8 ? C::SMEM_BYTES_I8 : C::SMEM_BYTES;
     auto run = [&](auto kern) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
-        kern<<<grid, pair::PAIR_THREADS, C::SMEM_BYTES, stream>>>(pa, pb, ty, la, lb, pbt, lbt, p);
+        kern<<<grid, g.i8 ? pair::PAIR_THREADS_I8 : pair::PAIR_THREADS, smem, stream>>>(pa, pb, ty, la, lb, pbt,
+                                                                                          lbt, p);
         return cudaGetLastError();
     };
+    if (g.i8) {
+        if (g.lora_r > 0) return cudaErrorNotSupported;
+        if (g.a) return run(pair::gemm_tc_pair_kernel<BN, true, 0, false, true>);
+        if (p.act == 1) return run(pair::gemm_tc_pair_kernel<BN, false, 1, false, true>);
+        if (p.act == 2) return run(pair::gemm_tc_pair_kernel<BN, false, 2, false, true>);
+        return run(pair::gemm_tc_pair_kernel<BN, false, 0, false, true>);
+    }
     if (g.a) return run(pair::gemm_tc_pair_kernel<BN, true, 0, false>);
     if (g.lora_r > 0) {
         if (p.act == 1) return run(pair::gemm_tc_pair_kernel<BN, false, 1, true>);
@@ -1010,6 +1287,9 @@ cudaError_t launch_pair(const GemmArgs &g, TcParams p, int sms, cudaStream_t str
 cudaError_t launch_gemm_tc(const GemmArgs &g, cudaStream_t stream)
 {
     if (g.m == 0 || g.n == 0) return cudaSuccess;
+    // int8 codes: the CTA-pair kernel widens them on chip; at most 128 rows take the
+    // legacy int8 MMA kernel
+    if (g.i8 && g.m <= BM) return launch_gemm_imma(g, stream);
     CUtensorMap ta, tb;
     if (!make_map(&ta, g.qx, g.m, g.kpad, g.ldqx, BM) || !make_map(&tb, g.qw, g.n, g.kpad, g.ldqw, BN))
         return cudaErrorInvalidValue;
@@ -1031,7 +1311,7 @@ cudaError_t launch_gemm_tc(const GemmArgs &g, cudaStream_t stream)
     p.vec_cols = (reinterpret_cast<uintptr_t>(g.sw) % 16 == 0) && (reinterpret_cast<uintptr_t>(g.bias) % 16 == 0);
     const int sms = sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
-    if (g.m > BM || g.lora_r > 0) {  // (the LoRA chunk exists in the pair kernel only)
+    if (g.m > BM || g.lora_r > 0 || g.i8) {  // (the LoRA chunk and int8 operands exist in the pair kernel only)
         // CTA pairs on 256 x 256 tiles. (224-wide tiles fill the last wave better on
         // paper but measured no faster on the DiT shapes: each chunk already runs at
         // close to the tensor peak and per-tile costs do not shrink with the width.)

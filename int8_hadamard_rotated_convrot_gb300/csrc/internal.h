@@ -39,6 +39,7 @@ struct GemmArgs {
     int64_t ldy;
     int32_t *dev_status;
     int32_t act;       // convrot_activation applied to Y (not to raw int32 output)
+    int32_t i8;        // 1: qx and qw hold int8 codes; 0: bf16 codes
     // LoRA side branch (bf16 codes only): Y += T_ext B_ext^T before the activation
     int32_t lora_r;          // 0: none
     const void *lora_t;      // T_ext bf16 [m, lora_ldt]

@@ -275,9 +275,10 @@ def test_gemm_identical_codes_bit_exact(m, n, k, G, codes):
     parity.check_y_same_codes(Y0.cpu().numpy(), Y64n, A_ref, sx, sw, None)
 
 
+@pytest.mark.parametrize("codes", GEMM_CODES, ids=GEMM_IDS)
 @pytest.mark.parametrize("m,n,act", [(512, 10240, 0), (512, 13468, 2), (300, 10112, 1), (512, 9984, 0),
                                      (768, 9984, 0)])
-def test_gemm_split_last_wave_bit_exact(m, n, act):
+def test_gemm_split_last_wave_bit_exact(m, n, act, codes):
     """Shapes whose last, partial wave of 256 x 256 tiles is split along N
     into items, on a 152-SM GB300: 80 tiles (4 past 76 pairs: 32-wide items),
     106 tiles (30 past: 128-wide items, the ragged last column of tiles among
@@ -291,8 +292,8 @@ def test_gemm_split_last_wave_bit_exact(m, n, act):
     sx = rng.uniform(0.001, 1.0, m).astype(np.float32)
     sw = rng.uniform(0.0001, 0.01, n).astype(np.float32)
     b = rng.standard_normal(n).astype(np.float32)
-    px = cr.packed_from_codes(to_dev(Qx), to_dev(sx), 64, cr.CODES_BF16)
-    pw = cr.packed_from_codes(to_dev(Qw), to_dev(sw), 64, cr.CODES_BF16)
+    px = cr.packed_from_codes(to_dev(Qx), to_dev(sx), 64, codes)
+    pw = cr.packed_from_codes(to_dev(Qw), to_dev(sw), 64, codes)
     Abig = torch.full((m + 1, (n + 7) // 4 * 4), -5, dtype=torch.int32, device="cuda")
     A = cr.convrot_gemm_i32(px, pw, out=Abig[:m, :n])
     Ybig = torch.full((m + 1, (n + 7) // 4 * 4), -3.0, dtype=torch.float32, device="cuda")
@@ -379,12 +380,14 @@ def sample_rows(m: int, n_rows: int, seed: int = 123) -> np.ndarray:
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("name", FULL)
-def test_full_size_sampled(name):
+@pytest.mark.parametrize("name,codes", [(n, cr.CODES_BF16) for n in FULL] + [("mlp_up", cr.CODES_I8),
+                                                                         ("mlp_down", cr.CODES_I8)],
+                         ids=FULL + ["mlp_up-i8", "mlp_down-i8"])
+def test_full_size_sampled(name, codes):
     """Full workload on the GPU in the bench's configuration: the pack against the
-    oracle on every row, Y on sampled rows plus the tail."""
+    oracle on every row, Y on sampled rows plus the tail. The I8 cases store the
+    page's int8 codes and run the tensor-core kernel that widens them on chip."""
     wl = inputs.WORKLOADS[name]
-    codes = GEMM_CODES[-1]
     X, W, b = inputs.activations(wl), inputs.weights(wl), inputs.bias(wl)
     px = cr.convrot_pack_activations(to_dev(X), wl.G, codes)
     pw = cr.convrot_quantize_weights(to_dev(W), wl.G, codes)
@@ -417,7 +420,8 @@ def test_full_size_sampled(name):
     A_ref = oracle.gemm_i32(Qx_ref, Qw_ref, wl.k)
     _, Y64_ref = oracle.reconstruct(A_ref, sx_ref, sw_ref, b)
     e2e = parity.check_y_end_to_end(Y_rows, Y64_ref, (qx_gpu, Qx_ref), (qw_gpu, Qw_ref), sx_gpu, sw_gpu)
-    parity.record(name, qx_codes=int(wl.m * wl.k), qx_flips_all_rows=pack_flips, qw_codes=int(wl.n * wl.k),
+    parity.record(name + ("" if codes == cr.CODES_BF16 else " (I8 codes)"), qx_codes=int(wl.m * wl.k),
+                  qx_flips_all_rows=pack_flips, qw_codes=int(wl.n * wl.k),
                   qw_flips=w_flips, y_rows=int(rows.size), **e2e)
 
 
