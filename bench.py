@@ -43,6 +43,9 @@ def parse():
     ap.add_argument("--workload", default="mlp_up")
     ap.add_argument("--codes", choices=["auto", "i8", "bf16"], default="auto")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--fused-pack", action="store_true",
+                    help="MLP pair: pack the up projection's output in its epilogue (convrot_linear_act_pack) "
+                         "instead of a separate pack launch")
     ap.add_argument("--eager", action="store_true",
                     help="launch the timed steps one call at a time instead of replaying them as one CUDA graph")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
@@ -292,6 +295,12 @@ def run_ours(args):
     # a stream of its own: the timed steps are captured into a CUDA graph on it
     stream = torch.cuda.Stream(dev)
     torch.cuda.synchronize(dev)
+    # MLP pair with --fused-pack: the down projection's pack fused into the up projection
+    # (rotation and row absmax in its epilogue, then a light quantize launch)
+    fused = bool(wl.down_n) and args.fused_pack
+    if fused:
+        works = [torch.empty((cr.linear_pack_work_bytes(wl.m, stages[0].n),), dtype=torch.uint8, device=dev)
+                 for _ in range(R)]
     if wl.lora_r:  # runtime LoRA on the first linear: T from the unrotated X, one extra GEMM chunk
         A_l, B_l = inputs.lora_weights(wl)
         A_l = cr.convrot_lora_prepare_down(torch.from_numpy(A_l).to(dev))
@@ -305,7 +314,15 @@ def run_ours(args):
         for s_i, st in enumerate(stages):
             def pack(h=h, s_i=s_i):
                 cr.convrot_pack_activations(h, wl.G, codes, out=pxs[s_i][j], stream=stream)
-            if wl.lora_r and s_i == 0:
+            if fused and s_i == 1:
+                ops.append(("gemm", lambda s_i=s_i, st=st: cr.convrot_linear_act(
+                    pxs[s_i][j], pws[s_i][j], biases[s_i], st.act, out=Ys[s_i][j], stream=stream)))
+            elif fused and s_i == 0:
+                ops.append(("pack", pack))
+                ops.append(("gemm_pack", lambda st=st: cr.convrot_linear_act_pack(
+                    pxs[0][j], pws[0][j], biases[0], st.act, wl.G, codes, out=pxs[1][j], work=works[j],
+                    stream=stream)))
+            elif wl.lora_r and s_i == 0:
                 ops.append(("lora_down", lambda h=h: cr.convrot_lora_down(h, A_l, out=T_ext[j], stream=stream)))
                 ops.append(("pack", pack))
                 ops.append(("gemm", lambda s_i=s_i, st=st: cr.convrot_linear_lora(
@@ -498,12 +515,17 @@ def run_ours(args):
     value = job_tops(world, ops, ms_step)
     gemm_avg = kern_ms["gemm"]
     pack_avg = kern_ms["pack"]
+    fused_avg = kern_ms.get("gemm_pack")
     pk = peaks()
     gemm_tops = ops / (gemm_avg * 1e-3) / 1e12
     # algorithmic bytes of a pack: 4 B read + 1 B code written per element + 4 B scale per row
     # (the page's I8 codes); the bytes this launch actually stores (bf16 codes: 2 B) beside them
-    pack_bytes = sum(wl.m * (5 * st.k + 4) for st in stages)
-    stored_pack_bytes = sum(wl.m * (4 * st.k + code_b * st.k + 4) for st in stages)
+    # (fused MLP pair: only the activation pack is a pack launch; the hidden one is in gemm_pack)
+    pack_stages = stages[:1] if fused else stages
+    pack_bytes = sum(wl.m * (5 * st.k + 4) for st in pack_stages)
+    stored_pack_bytes = sum(wl.m * (4 * st.k + code_b * st.k + 4) for st in pack_stages)
+    if fused:  # the GEMM figure covers the down projection alone; the up one is inside gemm_pack
+        gemm_tops = 2 * wl.m * stages[1].n * stages[1].k / (gemm_avg * 1e-3) / 1e12
     pack_gbs = pack_bytes / (pack_avg * 1e-3) / 1e9
     stored_pack_gbs = stored_pack_bytes / (pack_avg * 1e-3) / 1e9
     first_pack_bytes = wl.m * (5 * stages[0].k + 4)
@@ -529,6 +551,10 @@ def run_ours(args):
                    "kernel_timing": "each launch of the step repeated K times back to back over the rotating "
                                     "sets, CUDA events around the batch (pack_ms, gemm_ms and the rooflines)"},
         "pack_gbs": pack_gbs, "pack_ms": pack_avg, "gemm_ms": gemm_avg, "gemm_tops": gemm_tops,
+        **({"gemm_pack_ms": fused_avg,
+            "fused": "up projection + GELU + the down projection's rotation and row absmax in one GEMM, then a "
+                     "quantize launch (gemm_pack_ms, both); gemm_ms and gemm_tops: the down projection"}
+           if fused else {}),
         **({"lora_down_ms": kern_ms["lora_down"],
             "lora": f"rank {wl.lora_r}, scale {wl.lora_scale:g}: T = X A^T in its own kernel (lora_down_ms), "
                     "the correction as an extra fp32 chunk of the GEMM (in gemm_ms); its own "
@@ -557,6 +583,7 @@ def run_ours(args):
                 "pipelining": "H2D of step i+1 and D2H of step i overlap compute on separate streams",
                 "h2d_bytes_per_step": wl.m * wl.k * 4, "d2h_bytes_per_step": wl.m * n_out * 4,
                 "ms_per_step": e2e_ms},
+        # (fused MLP pair: pack, GEMM, quantize, GEMM; its cudaMemsetAsync is a runtime memset node)
         "gpu_launches": (2 * len(stages) + (1 if wl.lora_r else 0)) * args.steps,
         "clocks": clk,
     }

@@ -174,6 +174,38 @@ convrot_status convrot_linear_act(const convrot_packed *x, const convrot_packed 
                                   cudaStream_t stream);
 
 /*
+ * The linear with an activation, followed by the pack of its output for the
+ * next linear ("Runtime activation quantization" applied to H): out_h receives
+ * the codes and row scales of H = act(x w^T linear) rotated with group size G,
+ * exactly what convrot_linear_act into an [m, n] buffer followed by
+ * convrot_pack_activations(H, G) gives (H is the same; codes may differ only
+ * at exact-tie ulps of the rotation's fp32 summation order). No counterpart
+ * on the page as one call: it is the page's pack of the next layer's input,
+ * moved into this layer's epilogue (a DiT MLP's up projection feeding its
+ * down projection).
+ *   act, bias        as for convrot_linear_act.
+ *   G                the next linear's group size: 4^n, G | n (n = w->rows).
+ *   work, work_bytes device workspace, 256-byte aligned, at least
+ *                    convrot_linear_pack_work_bytes(m, n) bytes; it holds the
+ *                    rotated H and its row maxima; its contents are undefined
+ *                    afterwards and need no initialization.
+ *   out_h            caller-filled q/scale/ldq/codes as for
+ *                    convrot_pack_activations (ldq >= convrot_ldq(n));
+ *                    receives rows = m, k = n, group_size = G.
+ * Fused form (bf16 codes, n % 256 == 0, G <= 256): the GEMM's epilogue applies
+ * the activation, the rotation (a 256-column output tile row is whole groups)
+ * and an atomic row absmax, and stores the rotated values to work; a second
+ * launch quantizes them (reading the most recently stored columns first, while
+ * they are still in L2). Other requests run the linear into work and then the
+ * pack. Errors as for convrot_linear_act and convrot_pack_activations;
+ * CONVROT_ERR_INVALID_ARG for a missing or short work buffer.
+ */
+int64_t convrot_linear_pack_work_bytes(int64_t m, int64_t n);
+convrot_status convrot_linear_act_pack(const convrot_packed *x, const convrot_packed *w, const float *bias,
+                                       int32_t act, int32_t G, void *work, int64_t work_bytes, convrot_packed *out_h,
+                                       int32_t *dev_status, cudaStream_t stream);
+
+/*
  * Runtime LoRA side branch (page "INT8 Convrot Safetensors", "Backend
  * support", paragraph on adapters): the INT8 weights stay as they are, and
  * the adapter's correction is computed from the original, unrotated

@@ -30,6 +30,8 @@ EXPORTED = [
     "convrot_pack_activations",
     "convrot_linear",
     "convrot_linear_act",
+    "convrot_linear_pack_work_bytes",
+    "convrot_linear_act_pack",
     "convrot_lora_cols",
     "convrot_lora_prepare",
     "convrot_lora_prepare_down",
@@ -90,6 +92,10 @@ def load() -> ctypes.CDLL:
         lib.convrot_linear.restype = ctypes.c_int
         lib.convrot_linear_act.argtypes = [P, P, vp, i32, vp, i64, vp, vp]
         lib.convrot_linear_act.restype = ctypes.c_int
+        lib.convrot_linear_pack_work_bytes.argtypes = [i64, i64]
+        lib.convrot_linear_pack_work_bytes.restype = i64
+        lib.convrot_linear_act_pack.argtypes = [P, P, vp, i32, i32, vp, i64, P, vp, vp]
+        lib.convrot_linear_act_pack.restype = ctypes.c_int
         lib.convrot_lora_cols.argtypes = [i32]
         lib.convrot_lora_cols.restype = i64
         lib.convrot_lora_prepare.argtypes = [vp, i64, i32, i64, ctypes.c_float, vp, i64, vp]
@@ -235,6 +241,36 @@ def convrot_linear_act(x: Packed, w: Packed, bias: torch.Tensor | None, act: int
     _check(load().convrot_linear_act(ctypes.byref(xs), ctypes.byref(ws), _ptr(bias), int(act), _ptr(out),
                                      out.stride(0) if out.dim() == 2 else 0, _ptr(dev_status),
                                      _stream(stream)), "convrot_linear_act")
+    return out
+
+
+def linear_pack_work_bytes(m: int, n: int) -> int:
+    """Bytes of the workspace convrot_linear_act_pack needs for an [m, n] output."""
+    return int(load().convrot_linear_pack_work_bytes(int(m), int(n)))
+
+
+def convrot_linear_act_pack(x: Packed, w: Packed, bias: torch.Tensor | None, act: int, G: int,
+                            codes: int = CODES_BF16, out: Packed | None = None, work: torch.Tensor | None = None,
+                            dev_status: torch.Tensor | None = None, stream=None) -> Packed:
+    """The linear with an activation, then the pack of its output H = act(...) for the next
+    linear with group size G: the same codes and scales as convrot_linear_act followed by
+    convrot_pack_activations, with the rotation and row absmax in the GEMM's epilogue.
+    ``work`` (uint8 CUDA tensor of linear_pack_work_bytes(m, n) bytes) is allocated here
+    when not given."""
+    if bias is not None and (bias.dtype != torch.float32 or not bias.is_cuda):
+        raise TypeError("bias must be a float32 CUDA tensor")
+    m, n = x.rows, w.rows
+    need = linear_pack_work_bytes(m, n)
+    if work is None:
+        work = torch.empty((max(need, 1),), dtype=torch.uint8, device=x.q.device)
+    elif work.dtype != torch.uint8 or not work.is_cuda or work.dim() != 1 or work.numel() < need:
+        raise ValueError(f"work must be a 1-D uint8 CUDA tensor of at least {need} bytes")
+    out = out or empty_packed(m, n, codes, x.q.device)
+    xs, ws, os_ = x.struct(), w.struct(), out.struct()
+    _check(load().convrot_linear_act_pack(ctypes.byref(xs), ctypes.byref(ws), _ptr(bias), int(act), int(G),
+                                          _ptr(work), int(work.numel()), ctypes.byref(os_), _ptr(dev_status),
+                                          _stream(stream)), "convrot_linear_act_pack")
+    out.rows, out.k, out.group_size = int(os_.rows), int(os_.k), int(os_.group_size)
     return out
 
 

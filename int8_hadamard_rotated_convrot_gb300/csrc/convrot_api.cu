@@ -238,9 +238,83 @@ convrot_status run_gemm(const convrot_packed *x, const convrot_packed *w, const 
     return e == cudaSuccess ? CONVROT_OK : CONVROT_ERR_CUDA;
 }
 
+// Work layout of convrot_linear_act_pack: H [m, ldh] fp32 (ldh = n rounded up to
+// 64) at offset 0, then the row maxima [m] (32-bit words), each part 256-byte aligned.
+int64_t pack_work_ldh(int64_t n) { return (n + 63) / 64 * 64; }
+int64_t round256(int64_t b) { return (b + 255) / 256 * 256; }
+int64_t pack_work_h_bytes(int64_t m, int64_t n) { return round256(m * pack_work_ldh(n) * 4); }
+
 }  // namespace
 
 extern "C" {
+
+int64_t convrot_linear_pack_work_bytes(int64_t m, int64_t n)
+{
+    if (m < 0 || n < 1 || n > CONVROT_MAX_K) return 0;
+    return pack_work_h_bytes(m, n) + round256(m * 4);
+}
+
+convrot_status convrot_linear_act_pack(const convrot_packed *x, const convrot_packed *w, const float *bias,
+                                       int32_t act, int32_t G, void *work, int64_t work_bytes, convrot_packed *out_h,
+                                       int32_t *dev_status, cudaStream_t stream)
+{
+    if (!x || !w || !out_h) return CONVROT_ERR_INVALID_ARG;
+    const int64_t m = x->rows, n = w->rows;
+    if (m < 0 || n < 0) return CONVROT_ERR_INVALID_ARG;
+    int log4g = 0;
+    // the output is the next linear's input: n is that linear's k
+    convrot_status st = check_k_g(n, G, &log4g);
+    if (st != CONVROT_OK) return st;
+    st = check_packed_buffers(out_h, m, n);
+    if (st != CONVROT_OK) return st;
+    const int64_t ldh = pack_work_ldh(n);
+    if (m > 0) {
+        if (!work || work_bytes < convrot_linear_pack_work_bytes(m, n)) return CONVROT_ERR_INVALID_ARG;
+        if (!aligned(work, 256)) return CONVROT_ERR_ALIGNMENT;
+    }
+    float *H = static_cast<float *>(work);
+    st = check_gemm(x, w, bias, m > 0 ? H : nullptr, nullptr, ldh, act, dev_status);
+    if (st != CONVROT_OK) return st;
+    if (m == 0) {
+        out_h->rows = 0;
+        out_h->k = n;
+        out_h->group_size = G;
+        return CONVROT_OK;
+    }
+    const bool fused = x->codes == CONVROT_CODES_BF16 && n % 256 == 0 && G <= 256;
+    if (!fused) {  // the same result in two launches: the linear into the work buffer, then the pack
+        st = run_gemm(x, w, bias, H, nullptr, ldh, act, dev_status, stream);
+        if (st != CONVROT_OK) return st;
+        return pack_rows(H, m, n, ldh, G, out_h, dev_status, stream);
+    }
+    uint32_t *rowmax = reinterpret_cast<uint32_t *>(static_cast<char *>(work) + pack_work_h_bytes(m, n));
+    if (cudaMemsetAsync(rowmax, 0, static_cast<size_t>(m) * 4, stream) != cudaSuccess) return CONVROT_ERR_CUDA;
+    convrot::GemmArgs g{};
+    g.qx = x->q;
+    g.ldqx = x->ldq;
+    g.qw = w->q;
+    g.ldqw = w->ldq;
+    g.m = m;
+    g.n = n;
+    g.kpad = static_cast<int32_t>(convrot_ldq(x->k));
+    g.sx = x->scale;
+    g.sw = w->scale;
+    g.bias = bias;
+    g.a = reinterpret_cast<int32_t *>(H);  // the rotated values, stored as 32-bit words
+    g.ldy = ldh;
+    g.dev_status = dev_status;
+    g.act = act;
+    g.rot_digits = log4g;
+    g.rot_rowmax = rowmax;
+    if (convrot::launch_gemm_tc(g, stream) != cudaSuccess) return CONVROT_ERR_CUDA;
+    out_h->rows = m;
+    out_h->k = n;
+    out_h->group_size = G;
+    return convrot::launch_requant(H, ldh, rowmax, m, static_cast<int32_t>(n), log4g, out_h->q, out_h->ldq,
+                                   out_h->scale, out_h->codes == CONVROT_CODES_BF16, stream) == cudaSuccess
+               ? CONVROT_OK
+               : CONVROT_ERR_CUDA;
+}
 
 int64_t convrot_ldq(int64_t k) { return k <= 0 ? 0 : ((k + 127) / 128) * 128; }
 

@@ -119,6 +119,11 @@ struct TcParams {
     // split along N into tail_split items (1, 2, 4 or 8)
     int64_t full_tiles;
     int32_t tail_split;
+    // pair kernel, kRot: the output's rotation (H4 along its rot_digits lowest base-4
+    // digits, unnormalized) is applied in the epilogue, and each row's absmax of it is
+    // folded into rowmax (fp32 bits, atomicMax); the rotated values go out through y_raw
+    uint32_t *rowmax;
+    int32_t rot_digits;
 };
 
 
@@ -487,6 +492,45 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 
 // ---------------------------------------------------------------------------
+// Rotation in the epilogue (the next linear's pack fused into this one's
+// output, "Runtime activation quantization" of the page applied to H). A
+// 256-column tile row is one group of G <= 256; its in-group index is
+// 64 part + 16 a + 4 b + c for the warp's 64-column slice `part`. H4 along a
+// base-4 digit in the mirror form of 2 H4 (every row all ones but a -1 at the
+// mirrored place): y_i = (x_0 + x_1 + x_2 + x_3) - 2 x_{3-i}, each output at
+// its own index, unnormalized (2^n times the rotation; the scale takes 2^-n).
+
+__device__ __forceinline__ void h4_mirror(float &a0, float &a1, float &a2, float &a3)
+{
+    const float s = (a0 + a1) + (a2 + a3);
+    const float y0 = fmaf(-2.0f, a3, s), y1 = fmaf(-2.0f, a2, s);
+    const float y2 = fmaf(-2.0f, a1, s), y3 = fmaf(-2.0f, a0, s);
+    a0 = y0;
+    a1 = y1;
+    a2 = y2;
+    a3 = y3;
+}
+
+// Digits 0, 1 and 2 (those below nd) of the thread's 64 consecutive values.
+__device__ __forceinline__ void rot_slice_digits(float (&h)[64], int nd)
+{
+    if (nd >= 1) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) h4_mirror(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
+    }
+    if (nd >= 2) {
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) h4_mirror(h[16 * a + c], h[16 * a + 4 + c], h[16 * a + 8 + c], h[16 * a + 12 + c]);
+    }
+    if (nd >= 3) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) h4_mirror(h[j], h[16 + j], h[32 + j], h[48 + j]);
+    }
+}
+
+// ---------------------------------------------------------------------------
 // CTA-pair variant (tcgen05 cta_group::2): two CTAs of a cluster compute a
 // 256 x 256 tile. Each CTA loads its own 128 rows of A and its own 128 rows
 // of B (half of the tile's N) into a 6-stage ring of 32 KB stages; the even
@@ -709,7 +753,11 @@ static_assert(PAIR_EPI_WARPS * PAIR_NBUF * PAIR_BUF_BYTES == PAIR_OUT_BYTES, "st
 // and the MMA runs kind::f16 on f16 operands.
 constexpr int kConvWarps = 6;
 
-template <int BN, bool kRawInt32, int kAct, bool kLora, bool kI8 = false>
+// kRot: the output is the next linear's input; each tile row (one group) is
+// rotated in the epilogue, its absmax folded into rowmax, and the rotated
+// values stored through y_raw (tmY then maps them as 32-bit words). Whole
+// tiles only: the last wave is not split along N.
+template <int BN, bool kRawInt32, int kAct, bool kLora, bool kI8 = false, bool kRot = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kI8 ? PAIR_THREADS_I8 : PAIR_THREADS, 1)
     gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmLa,
@@ -718,6 +766,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kI8 ? PAIR_THREADS_I
 {
     using C = Cfg<BN>;
     static_assert(!(kI8 && kLora), "the LoRA chunk is bf16: it runs with bf16 codes only");
+    static_assert(!kRot || (!kRawInt32 && !kLora && BN == 256), "the rotation epilogue stores whole 256-column rows");
     constexpr int STAGES = kI8 ? C::STAGES_I8 : C::STAGES, RSTAGES = kI8 ? C::RAW_STAGES : 0;
     constexpr int STAGE_BYTES = C::STAGE_BYTES, A_BYTES = C::A_BYTES, BNP = C::BNP, BNC = C::BNC;
     extern __shared__ uint8_t smem_raw[];
@@ -736,7 +785,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kI8 ? PAIR_THREADS_I
     auto raw_empty = [&](int r) { return bars + 8u * (2 * STAGES + 5 + RSTAGES + r); };
     // kI8, odd CTA: its converter warps arrive here; one thread forwards each phase to the even CTA
     auto conv_done = [&](int s) { return bars + 8u * (2 * STAGES + 5 + 2 * RSTAGES + s); };
-    constexpr int kSlotOff = kI8 ? 8 * (3 * STAGES + 5 + 2 * RSTAGES) + 8 : 160;
+    // kRot: the four epilogue warps of TMEM lane quadrant q exchange their slices through these
+    constexpr int kXch0 = 2 * STAGES + 5 + (kI8 ? STAGES + 2 * RSTAGES : 0);
+    auto xch_bar = [&](int q) { return bars + 8u * (kXch0 + q); };
+    constexpr int kSlotOff = (kI8 || kRot) ? 8 * (kXch0 + (kRot ? 4 : 0)) + 8 : 160;
     static_assert(kSlotOff + 8 <= BAR_BYTES, "barriers, TMEM slot and abort flag fit their region");
     uint8_t *const slots = gbase + (out_base - base) + PAIR_OUT_BYTES + kSlotOff;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(slots);
@@ -768,6 +820,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kI8 ? PAIR_THREADS_I
             mbar_init(accf_bar(b), 1);
             mbar_init(acce_bar(b), 2 * PAIR_EPI_WARPS);
         }
+        if constexpr (kRot)
+            for (int q = 0; q < 4; ++q) mbar_init(xch_bar(q), 4);
         if constexpr (kLora) {
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmLa)) : "memory");
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmLb)) : "memory");
@@ -1049,6 +1103,90 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kI8 ? PAIR_THREADS_I
         uint32_t store_iter = 0;
         uint32_t chunk_iter = 0;
         bool ok = true;
+        uint32_t xch_phase = 0;
+        // kRot: y = act(A s_x s_w + b) for the warp's 32 rows x 64 columns, rotated
+        // (digits 0-2 in registers, digit 3 across the quadrant's four slices through
+        // the staging buffers), absmax into rowmax, then the rotated values stored.
+        // False if a partner warp's exchange did not come within the bounded wait.
+        auto rot_store = [&](int64_t row0, int64_t col0, int32_t (&acc)[PAIR_COLS]) -> bool {
+            const int64_t row = row0 + lane;
+            const float sxr = row < p.m ? p.sx[row] : 0.0f;
+            float h[PAIR_COLS];
+#pragma unroll
+            for (int c = 0; c < PAIR_COLS / 4; ++c) {
+                const int64_t col = col0 + 4 * c;  // n is a multiple of 256 in this form
+                float4 sw4, b4 = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (p.vec_cols) {
+                    sw4 = __ldg(reinterpret_cast<const float4 *>(p.sw + col));
+                    if (p.bias) b4 = __ldg(reinterpret_cast<const float4 *>(p.bias + col));
+                } else {
+                    sw4 = make_float4(__ldg(p.sw + col), __ldg(p.sw + col + 1), __ldg(p.sw + col + 2), __ldg(p.sw + col + 3));
+                    if (p.bias)
+                        b4 = make_float4(__ldg(p.bias + col), __ldg(p.bias + col + 1), __ldg(p.bias + col + 2),
+                                         __ldg(p.bias + col + 3));
+                }
+                h[4 * c] = apply_act_t<kAct>(fmaf(static_cast<float>(acc[4 * c]) * sxr, sw4.x, b4.x));
+                h[4 * c + 1] = apply_act_t<kAct>(fmaf(static_cast<float>(acc[4 * c + 1]) * sxr, sw4.y, b4.y));
+                h[4 * c + 2] = apply_act_t<kAct>(fmaf(static_cast<float>(acc[4 * c + 2]) * sxr, sw4.z, b4.z));
+                h[4 * c + 3] = apply_act_t<kAct>(fmaf(static_cast<float>(acc[4 * c + 3]) * sxr, sw4.w, b4.w));
+            }
+            rot_slice_digits(h, p.rot_digits);
+            if (p.rot_digits >= 4) {
+                const uint32_t xb = xch_bar(q);
+                auto sync4 = [&]() {  // the quadrant's four warps reach the same point (bounded)
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(xb);
+                    const bool got = mbar_wait(xb, xch_phase);
+                    xch_phase ^= 1u;
+                    return __all_sync(0xffffffffu, got);
+                };
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+                    __syncwarp();
+#pragma unroll
+                    for (int c4 = 0; c4 < 4; ++c4)
+                        asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(box_addr<16>(out_smem, lane, c4)),
+                                     "f"(h[16 * r + 4 * c4]), "f"(h[16 * r + 4 * c4 + 1]), "f"(h[16 * r + 4 * c4 + 2]),
+                                     "f"(h[16 * r + 4 * c4 + 3])
+                                     : "memory");
+                    if (!sync4()) return false;
+#pragma unroll
+                    for (int c4 = 0; c4 < 4; ++c4) {
+                        float x[4][4];
+#pragma unroll
+                        for (int pp = 0; pp < 4; ++pp) {
+                            if (pp == part) {
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) x[pp][e] = h[16 * r + 4 * c4 + e];
+                            } else {
+                                const uint32_t pb = out_base + (4 * pp + q) * PAIR_NBUF * PAIR_BUF_BYTES;
+                                asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                                             : "=f"(x[pp][0]), "=f"(x[pp][1]), "=f"(x[pp][2]), "=f"(x[pp][3])
+                                             : "r"(box_addr<16>(pb, lane, c4)));
+                            }
+                        }
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float sum = (x[0][e] + x[1][e]) + (x[2][e] + x[3][e]);
+                            // x_{3 - part}, selected without indexing by a runtime value
+                            const float mirror = part == 0 ? x[3][e] : part == 1 ? x[2][e] : part == 2 ? x[1][e] : x[0][e];
+                            h[16 * r + 4 * c4 + e] = fmaf(-2.0f, mirror, sum);
+                        }
+                    }
+                    if (!sync4()) return false;
+                }
+            }
+            float mx = 0.0f;
+#pragma unroll
+            for (int j = 0; j < PAIR_COLS; ++j) mx = fmaxf(mx, fabsf(h[j]));
+            if (row < p.m) atomicMax(p.rowmax + row, __float_as_uint(mx));
+#pragma unroll
+            for (int j = 0; j < PAIR_COLS; ++j) acc[j] = __float_as_int(h[j]);
+            store_tile_rows<true, 0, false, PAIR_COLS, PAIR_NBUF, PAIR_BW>(p, &tmY, out_smem, store_iter, row0, col0,
+                                                                           acc, lane);
+            return true;
+        };
         const int ncols = BNP - part * PAIR_COLS < PAIR_COLS ? (BNP - part * PAIR_COLS > 0 ? BNP - part * PAIR_COLS : 0)
                                                              : PAIR_COLS;
         for (int64_t t = pair_id; t < p.full_tiles && ok; t += n_pairs) {
@@ -1093,6 +1231,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kI8 ? PAIR_THREADS_I
                 __syncwarp();
                 if (lane == 0) arrive_remote(map_to_rank(acce_bar(buf), 0));
                 ++chunk_iter;
+            } else if constexpr (kRot) {
+                if (!rot_store(mt * 2 * BMC + static_cast<int64_t>(rank) * BMC + q * 32, nt * BNP + part * PAIR_COLS,
+                               acc)) {
+                    ok = false;
+                    break;
+                }
             } else {
                 store_tile_rows<kRawInt32, kAct, false, PAIR_COLS, PAIR_NBUF, PAIR_BW>(
                     p, &tmY, out_smem, store_iter, mt * 2 * BMC + static_cast<int64_t>(rank) * BMC + q * 32,
@@ -1148,6 +1292,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kI8 ? PAIR_THREADS_I
                     __syncwarp();
                     if (lane == 0) arrive_remote(map_to_rank(acce_bar(buf), 0));
                     ++chunk_iter;
+                } else if constexpr (kRot) {  // (whole tiles: tail_split is 1 in this form)
+                    if (!rot_store(mt * 2 * BMC + static_cast<int64_t>(rank) * BMC + q * 32,
+                                   nt * BNP + part * PAIR_COLS, acc)) {
+                        ok = false;
+                        break;
+                    }
                 } else {
                     store_tile_rows<kRawInt32, kAct, false, PAIR_COLS, PAIR_NBUF, PAIR_BW>(
                         p, &tmY, out_smem, store_iter, mt * 2 * BMC + static_cast<int64_t>(rank) * BMC + q * 32,
@@ -1245,7 +1395,7 @@ cudaError_t launch_pair(const GemmArgs &g, TcParams p, int sms, cudaStream_t str
     // more pairs. B (and the LoRA chunk's B_ext) then come in narrower boxes.
     const int64_t full = tiles / pairs * pairs, tail = tiles - full;
     int split = 1;
-    if (BN == 256 && tail > 0)
+    if (BN == 256 && tail > 0 && g.rot_digits == 0)  // (the rotation epilogue needs whole tiles)
         while (split < 8 && tail * split * 2 <= pairs) split *= 2;
     p.full_tiles = full;
     p.tail_split = split;
@@ -1264,6 +1414,14 @@ cudaError_t launch_pair(const GemmArgs &g, TcParams p, int sms, cudaStream_t str
                                                                                           lbt, p);
         return cudaGetLastError();
     };
+    if (g.rot_digits > 0) {
+        if (g.i8 || g.lora_r > 0 || !g.a || g.n % 256 != 0) return cudaErrorNotSupported;
+        p.rowmax = g.rot_rowmax;
+        p.rot_digits = g.rot_digits;
+        if (p.act == 1) return run(pair::gemm_tc_pair_kernel<BN, false, 1, false, false, true>);
+        if (p.act == 2) return run(pair::gemm_tc_pair_kernel<BN, false, 2, false, false, true>);
+        return run(pair::gemm_tc_pair_kernel<BN, false, 0, false, false, true>);
+    }
     if (g.i8) {
         if (g.lora_r > 0) return cudaErrorNotSupported;
         if (g.a) return run(pair::gemm_tc_pair_kernel<BN, true, 0, false, true>);
@@ -1311,7 +1469,7 @@ cudaError_t launch_gemm_tc(const GemmArgs &g, cudaStream_t stream)
     p.vec_cols = (reinterpret_cast<uintptr_t>(g.sw) % 16 == 0) && (reinterpret_cast<uintptr_t>(g.bias) % 16 == 0);
     const int sms = sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
-    if (g.m > BM || g.lora_r > 0 || g.i8) {  // (the LoRA chunk and int8 operands exist in the pair kernel only)
+    if (g.m > BM || g.lora_r > 0 || g.i8 || g.rot_digits > 0) {  // (LoRA, int8 operands, rotation: pair kernel only)
         // CTA pairs on 256 x 256 tiles. (224-wide tiles fill the last wave better on
         // paper but measured no faster on the DiT shapes: each chunk already runs at
         // close to the tensor peak and per-tile costs do not shrink with the width.)

@@ -24,6 +24,14 @@ struct PackArgs {
 
 cudaError_t launch_pack(const PackArgs &a, cudaStream_t stream);
 
+// Codes and scales of rows whose rotation was applied by the GEMM's epilogue
+// (GemmArgs::rot_digits): H_rot [rows, ldh] fp32 (unnormalized, 2^log4g times
+// the rotation) and rowmax [rows] (its absmax, fp32 bits) -> q, scale as the
+// pack writes them. Columns go from the last to the first, the order in which
+// the GEMM left them in L2; each H_rot line is discarded from L2 once read.
+cudaError_t launch_requant(const float *h_rot, int64_t ldh, const uint32_t *rowmax, int64_t rows, int32_t k,
+                           int32_t log4g, void *q, int64_t ldq, float *scale, int32_t bf16, cudaStream_t stream);
+
 struct GemmArgs {
     const void *qx;    // [m, ldqx] codes
     int64_t ldqx;
@@ -40,6 +48,11 @@ struct GemmArgs {
     int32_t *dev_status;
     int32_t act;       // convrot_activation applied to Y (not to raw int32 output)
     int32_t i8;        // 1: qx and qw hold int8 codes; 0: bf16 codes
+    // > 0: rotate the output in the epilogue along its rot_digits lowest base-4 digits
+    // (pair kernel, bf16 codes, n % 256 == 0), fold each row's absmax into rot_rowmax
+    // (fp32 bits, atomicMax; zeroed by the caller) and store the rotated values to `a`
+    int32_t rot_digits;
+    uint32_t *rot_rowmax;
     // LoRA side branch (bf16 codes only): Y += T_ext B_ext^T before the activation
     int32_t lora_r;          // 0: none
     const void *lora_t;      // T_ext bf16 [m, lora_ldt]

@@ -1078,7 +1078,76 @@ cudaError_t dispatch(const PackArgs &a, cudaStream_t stream)
     }
 }
 
+// Second half of a pack whose rotation and row absmax a GEMM epilogue already
+// applied: per element only the quantization ("Runtime activation
+// quantization": Q = round(X_rot / s), s = max |X_rot| / 127, here with the
+// unnormalized rotation and the scale's 2^-n as in scale_of). A warp takes one
+// row's 256 columns (8 lines of 128 bytes, two coalesced 16-byte loads a
+// lane), a CTA eight rows; each line is discarded from L2 once every lane has
+// used its values, so that its dirty copy is never written back. Column tiles
+// go from the last to the first: the GEMM stored them in that order of
+// recency, so the first ones read are still in L2.
+template <bool kBf16>
+__global__ void __launch_bounds__(256) requant_kernel(const float *__restrict__ h_rot, int64_t ldh,
+                                                      const uint32_t *__restrict__ rowmax, int64_t rows, int32_t k,
+                                                      int32_t log4g, void *q, int64_t ldq, float *scale)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t row_blocks = (rows + 7) / 8;
+    const int64_t ct = k / 256 - 1 - static_cast<int64_t>(blockIdx.x) / row_blocks;
+    const int64_t row = (static_cast<int64_t>(blockIdx.x) % row_blocks) * 8 + (threadIdx.x >> 5);
+    if (row >= rows) return;
+    float inv;
+    const float s = scale_of(__uint_as_float(rowmax[row]), log4g, &inv);
+    if (ct == 0 && lane == 0) scale[row] = s;
+    const uint32_t half_bits = 0x3f000000u | (__float_as_uint(inv) & kSign);
+    const float *src = h_rot + row * ldh + ct * 256;
+    const float4 v0 = __ldcs(reinterpret_cast<const float4 *>(src) + lane);        // columns 4 lane ..
+    const float4 v1 = __ldcs(reinterpret_cast<const float4 *>(src) + 32 + lane);   // columns 128 + 4 lane ..
+    float r[8] = {code_of(v0.x, inv, half_bits), code_of(v0.y, inv, half_bits), code_of(v0.z, inv, half_bits),
+                  code_of(v0.w, inv, half_bits), code_of(v1.x, inv, half_bits), code_of(v1.y, inv, half_bits),
+                  code_of(v1.z, inv, half_bits), code_of(v1.w, inv, half_bits)};
+    const int64_t c0 = ct * 256 + 4 * lane;
+    if constexpr (kBf16) {
+        __nv_bfloat16 *qrow = static_cast<__nv_bfloat16 *>(q) + row * ldq;
+        reinterpret_cast<uint2 *>(qrow + c0)[0] = make_uint2(__byte_perm(__float_as_uint(r[0]), __float_as_uint(r[1]), 0x7632),
+                                                             __byte_perm(__float_as_uint(r[2]), __float_as_uint(r[3]), 0x7632));
+        reinterpret_cast<uint2 *>(qrow + c0 + 128)[0] = make_uint2(
+            __byte_perm(__float_as_uint(r[4]), __float_as_uint(r[5]), 0x7632),
+            __byte_perm(__float_as_uint(r[6]), __float_as_uint(r[7]), 0x7632));
+    } else {
+        int8_t *qrow = static_cast<int8_t *>(q) + row * ldq;
+        constexpr float kMagic = 12582912.0f;
+        uint32_t b[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) b[e] = __float_as_uint(r[e] + kMagic);
+        reinterpret_cast<uint32_t *>(qrow + c0)[0] =
+            __byte_perm(__byte_perm(b[0], b[1], 0x0040), __byte_perm(b[2], b[3], 0x0040), 0x5410);
+        reinterpret_cast<uint32_t *>(qrow + c0 + 128)[0] =
+            __byte_perm(__byte_perm(b[4], b[5], 0x0040), __byte_perm(b[6], b[7], 0x0040), 0x5410);
+    }
+    // every lane has used its loaded values (the codes above depend on them): drop the lines
+    __syncwarp();
+    if (lane < 8) asm volatile("discard.global.L2 [%0], 128;" ::"l"(src + 32 * lane) : "memory");
+}
+
 }  // namespace
+
+cudaError_t launch_requant(const float *h_rot, int64_t ldh, const uint32_t *rowmax, int64_t rows, int32_t k,
+                           int32_t log4g, void *q, int64_t ldq, float *scale, int32_t bf16, cudaStream_t stream)
+{
+    if (rows == 0) return cudaSuccess;
+    if (k % 256 != 0) return cudaErrorInvalidValue;
+    const int64_t blocks = (rows + 7) / 8 * (k / 256);
+    if (blocks >= (int64_t{1} << 31)) return cudaErrorInvalidValue;
+    if (bf16)
+        requant_kernel<true><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(h_rot, ldh, rowmax, rows, k, log4g, q,
+                                                                                ldq, scale);
+    else
+        requant_kernel<false><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(h_rot, ldh, rowmax, rows, k, log4g, q,
+                                                                                 ldq, scale);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_pack(const PackArgs &a, cudaStream_t stream)
 {
