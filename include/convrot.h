@@ -43,7 +43,7 @@ extern "C" {
 typedef enum {
     CONVROT_OK = 0,
     CONVROT_ERR_INVALID_ARG = 1, /* null pointer, negative size, ld too small, mismatched operands */
-    CONVROT_ERR_GROUP_SIZE = 2,  /* G not 4^n (n >= 1), G does not divide k, or G > 4096 */
+    CONVROT_ERR_GROUP_SIZE = 2,  /* G not 4^n (n >= 1), G does not divide k, or G > 65536 */
     CONVROT_ERR_ALIGNMENT = 3,   /* a pointer or leading dimension breaks the alignment rules */
     CONVROT_ERR_K_RANGE = 4,     /* k < 1 or k > CONVROT_MAX_K */
     CONVROT_ERR_CUDA = 5,        /* a kernel launch failed */
@@ -56,8 +56,10 @@ typedef enum {
  * activation quantization" accumulates in signed 32-bit integers). */
 #define CONVROT_MAX_K 133144
 
-/* Largest group size the pack kernel supports (4^6). */
-#define CONVROT_MAX_GROUP 4096
+/* Largest group size: 4^8, the largest power of four that can divide a k
+ * within CONVROT_MAX_K (the page admits any power of four dividing the input
+ * features, "Checkpoint format"). */
+#define CONVROT_MAX_GROUP 65536
 
 /* Element type of the stored codes. Both hold the same integers in
  * [-127, 127]; BF16 represents every one of them exactly and is the operand
@@ -138,7 +140,7 @@ convrot_status convrot_quantize_weights(const float *W, int64_t n, int64_t k, in
  *   m      rows (tokens), m >= 0 (0: nothing is launched).
  *   k, G   as for convrot_quantize_weights.
  *   out_x  caller-filled q/scale/ldq/codes; receives rows = m, k, G.
- *   dev_status  device int32 or NULL; see convrot_linear. (For G <= 256 the
+ *   dev_status  device int32 or NULL; see convrot_linear. (For G <= 1024 the
  *               pack streams rows into shared memory with bulk copies and
  *               waits for them with a 4 s bound; the other forms never wait.)
  */

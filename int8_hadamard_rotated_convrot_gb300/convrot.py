@@ -22,7 +22,7 @@ NOALLOC_SCRATCH_BYTES = 32 << 20
 WAIT_LIMIT_NS = 4_000_000_000
 CODES_I8, CODES_BF16 = 0, 1
 MAX_K = 133144
-MAX_GROUP = 4096
+MAX_GROUP = 65536
 
 EXPORTED = [
     "convrot_ldq",

@@ -448,7 +448,7 @@ const char *convrot_status_string(convrot_status s)
     switch (s) {
     case CONVROT_OK: return "ok";
     case CONVROT_ERR_INVALID_ARG: return "invalid argument";
-    case CONVROT_ERR_GROUP_SIZE: return "group size must be 4^n (n >= 1, at most 4096) and divide k";
+    case CONVROT_ERR_GROUP_SIZE: return "group size must be 4^n (n >= 1, at most 65536) and divide k";
     case CONVROT_ERR_ALIGNMENT: return "pointer or leading dimension is not suitably aligned";
     case CONVROT_ERR_K_RANGE: return "k must be in [1, 133144]";
     case CONVROT_ERR_CUDA: return "CUDA launch failed";

@@ -1064,6 +1064,143 @@ cudaError_t launch_g256(const PackArgs &a, cudaStream_t stream)
     return launch_plan(pack_g256_kernel<N, kBf16>, Shape{Tile<N>::LB, 16}, a, stream);
 }
 
+// ---------------------------------------------------------------------------
+// Groups of 16384 and 65536 (4^7, 4^8; the page admits any power of four that
+// divides the row, "Checkpoint format"). R_G = H4^(x)(n-6) (x) R_4096: each
+// warp applies R_4096 to one 4096-element block with the generic layout above
+// (32 lanes x 32 slots, D, Walsh-Hadamard butterflies, the output D and Pi
+// left to the store), then H4 goes along the digits above the block in the
+// mirror form of 2 H4 (y_i = s - 2 x_{3-i}): digit 6 across the CTA's four
+// warps through shared memory, digit 7 (G = 65536) across four CTAs of the
+// cluster through distributed shared memory. The block's output D and Pi act
+// the same way in every block, so they commute with those digits.
+// A CTA is 128 threads and 16384 elements of a row; the row's CTAs form a
+// cluster (k / 16384 <= 8), which also gives the row its absmax.
+
+__device__ __forceinline__ float4 ld_cluster_f4(uint32_t addr)
+{
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
+// Output `idx` of the mirror form of 2 H4 along one digit, componentwise.
+__device__ __forceinline__ float4 h4_mirror_out(const float4 &x0, const float4 &x1, const float4 &x2, const float4 &x3,
+                                                int idx)
+{
+    const float4 &m = idx == 0 ? x3 : idx == 1 ? x2 : idx == 2 ? x1 : x0;
+    return make_float4(fmaf(-2.0f, m.x, (x0.x + x1.x) + (x2.x + x3.x)), fmaf(-2.0f, m.y, (x0.y + x1.y) + (x2.y + x3.y)),
+                       fmaf(-2.0f, m.z, (x0.z + x1.z) + (x2.z + x3.z)), fmaf(-2.0f, m.w, (x0.w + x1.w) + (x2.w + x3.w)));
+}
+
+constexpr int kBigThreads = 128;
+constexpr int kBigSmem = 4 * 32 * 32 * 16;  // one float4 per (warp, slot, lane): 64 KB
+
+template <bool kBf16, int kHigh>
+__global__ void __launch_bounds__(kBigThreads) pack_big_kernel(PackArgs a, int cl)
+{
+    extern __shared__ float4 xbuf[];
+    __shared__ float part[4];
+    __shared__ float cta_max;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint32_t crank;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(crank));
+    const int64_t row = blockIdx.x / cl;
+    const int64_t block = static_cast<int64_t>(crank) * 4 + warp;  // 4096-element block of the row
+    const Place<5, 32> pl(lane, 6, 1024);
+    const float4 *src = reinterpret_cast<const float4 *>(a.x + row * a.ldx) + block * 1024;
+    float4 v[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = __ldcs(src + pl.quad(j));
+    rotate<5, 32>(v, pl);
+    // digit 6: the CTA's four blocks
+    auto slot = [&](int w, int j) { return (w * 32 + j) * 32 + lane; };
+#pragma unroll
+    for (int j = 0; j < 32; ++j) xbuf[slot(warp, j)] = v[j];
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+        v[j] = h4_mirror_out(xbuf[slot(0, j)], xbuf[slot(1, j)], xbuf[slot(2, j)], xbuf[slot(3, j)], warp);
+    if constexpr (kHigh == 2) {
+        // digit 7: four CTAs of the cluster (ranks 4 g .. 4 g + 3 hold one group)
+        __syncthreads();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) xbuf[slot(warp, j)] = v[j];
+        cluster_sync_all();
+        const uint32_t g0 = crank & ~3u, me = crank & 3u;
+        const uint32_t base = static_cast<uint32_t>(__cvta_generic_to_shared(xbuf));
+        uint32_t rb[4];
+#pragma unroll
+        for (uint32_t r = 0; r < 4; ++r) {
+            uint32_t m;
+            asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(m) : "r"(base), "r"(g0 + r));
+            rb[r] = m;
+        }
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const uint32_t off = static_cast<uint32_t>(slot(warp, j)) * 16u;
+            v[j] = h4_mirror_out(ld_cluster_f4(rb[0] + off), ld_cluster_f4(rb[1] + off), ld_cluster_f4(rb[2] + off),
+                                 ld_cluster_f4(rb[3] + off), static_cast<int>(me));
+        }
+        cluster_sync_all();  // no CTA overwrites or leaves its buffer while another reads it
+    }
+    float m = absmax<32>(v);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, off));
+    if (lane == 0) part[warp] = m;
+    __syncthreads();
+    float amax = fmaxf(fmaxf(part[0], part[1]), fmaxf(part[2], part[3]));
+    if (cl > 1) {
+        if (threadIdx.x == 0) cta_max = amax;
+        cluster_sync_all();  // every CTA's cta_max is written
+        amax = 0.0f;
+        for (int r = 0; r < cl; ++r) amax = fmaxf(amax, ld_cluster_f32(cluster_smem_addr(&cta_max, r)));
+    }
+    float inv;
+    const float s = scale_of(amax, a.log4g, &inv);
+    if (crank == 0 && threadIdx.x == 0) a.scale[row] = s;
+    char *qblock = static_cast<char *>(a.q) + (row * a.ldq + block * 4096) * (kBf16 ? 2 : 1);
+    quantize_store<5, 32, kBf16>(v, pl, qblock, inv);
+    if (cl > 1) cluster_sync_all();  // no CTA leaves while another may still read its cta_max
+}
+
+template <bool kBf16, int kHigh>
+cudaError_t launch_big(const PackArgs &a, cudaStream_t stream)
+{
+    // a.k is a multiple of G >= 16384 and at most 131072 here
+    const int cl = a.k / 16384;
+    if (cl < 1 || cl > 8 || a.k % 16384 != 0) return cudaErrorInvalidValue;
+    auto kern = pack_big_kernel<kBf16, kHigh>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kBigSmem);
+    if (e != cudaSuccess) return e;
+    const int64_t max_rows = ((int64_t{1} << 31) - 1) / cl;
+    for (int64_t r0 = 0; r0 < a.rows; r0 += max_rows) {
+        PackArgs b = a;
+        b.rows = a.rows - r0 < max_rows ? a.rows - r0 : max_rows;
+        b.x = a.x + r0 * a.ldx;
+        b.q = static_cast<char *>(a.q) + r0 * a.ldq * (kBf16 ? 2 : 1);
+        b.scale = a.scale + r0;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(b.rows * cl), 1, 1);
+        cfg.blockDim = dim3(kBigThreads, 1, 1);
+        cfg.dynamicSmemBytes = kBigSmem;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = static_cast<unsigned>(cl);
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, kern, b, cl);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
 template <bool kBf16>
 cudaError_t dispatch(const PackArgs &a, cudaStream_t stream)
 {
@@ -1074,6 +1211,8 @@ cudaError_t dispatch(const PackArgs &a, cudaStream_t stream)
     case 4: return launch_g256<4, kBf16>(a, stream);
     case 5: return launch_g256<5, kBf16>(a, stream);                                 // G = 1024
     case 6: return launch_plan(pack_kernel<5, 32, kBf16>, Shape{5, 32}, a, stream);  // G = 4096
+    case 7: return launch_big<kBf16, 1>(a, stream);                                  // G = 16384
+    case 8: return launch_big<kBf16, 2>(a, stream);                                  // G = 65536
     default: return cudaErrorInvalidValue;
     }
 }

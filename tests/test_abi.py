@@ -71,6 +71,13 @@ def test_pack_rejects_bad_group(lib, G):
     assert pack(lib, G=G) == cr.ERR_GROUP_SIZE
 
 
+def test_group_size_limits(lib):
+    """4^8 = 65536 is the largest power of four dividing a k within the range; 4^9 is rejected."""
+    assert pack(lib, k=131072, ldx=131072, G=65536, out=packed(ldq=131072)) != cr.ERR_GROUP_SIZE
+    assert pack(lib, k=131072, ldx=131072, G=16384, out=packed(ldq=131072)) != cr.ERR_GROUP_SIZE
+    assert pack(lib, k=131072, ldx=131072, G=262144, out=packed(ldq=131072)) == cr.ERR_GROUP_SIZE
+
+
 def test_pack_rejects_group_not_dividing_k(lib):
     assert pack(lib, k=96, ldx=96, G=64) == cr.ERR_GROUP_SIZE
 

@@ -159,6 +159,41 @@ def test_pack_long_rows_use_clusters(G, k):
     parity.check_codes(codes_np(p), Q, v)
 
 
+@pytest.mark.parametrize("codes", CODES, ids=CODE_IDS)
+@pytest.mark.parametrize("G,k,m", [(16384, 16384, 37), (16384, 49152, 9), (16384, 131072, 5), (65536, 65536, 9),
+                                   (65536, 131072, 5)])
+def test_pack_large_groups(G, k, m, codes):
+    """G = 16384 and 65536 (4^7, 4^8): one CTA of four 4096-element blocks per
+    16384 elements, the digits above the block across warps and, for 65536,
+    across four CTAs of the row's cluster."""
+    rng = np.random.default_rng(G + k + m)
+    X = special_rows(rng, m, k)
+    p = gpu_pack(X, G, codes)
+    Q, s, v = oracle.pack_rows(X, G)
+    parity.check_scales(p.scale.cpu().numpy(), s)
+    parity.check_codes(codes_np(p), Q, v)
+    assert float(p.scale[0]) == 0.0
+
+
+def test_linear_end_to_end_group_16384():
+    """The linear on rows packed with G = 16384 against the oracle end to end."""
+    rng = np.random.default_rng(16384)
+    m, k, n, G = 200, 16384, 256, 16384
+    X = special_rows(rng, m, k)
+    W = (0.02 * rng.standard_normal((n, k))).astype(np.float32)
+    b = (0.01 * rng.standard_normal(n)).astype(np.float32)
+    px = cr.convrot_pack_activations(to_dev(X), G, cr.CODES_BF16)
+    pw = cr.convrot_quantize_weights(to_dev(W), G, cr.CODES_BF16)
+    Y = cr.convrot_linear(px, pw, to_dev(b))
+    torch.cuda.synchronize()
+    ref = oracle.linear(X, W, b, G)
+    Qw_ref, _, vw = oracle.pack_rows(W, G)
+    parity.check_codes(codes_np(pw), Qw_ref, vw)
+    e2e = parity.check_y_end_to_end(Y.cpu().numpy(), ref["Y64"], (codes_np(px), ref["Qx"]), (codes_np(pw), Qw_ref),
+                                    px.scale.cpu().numpy(), pw.scale.cpu().numpy())
+    parity.record("G = 16384, 200x16384x256", y_rows=m, **e2e)
+
+
 def test_quantize_weights_equals_pack():
     rng = np.random.default_rng(5)
     W = (0.02 * rng.standard_normal((300, 512))).astype(np.float32)

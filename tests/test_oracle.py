@@ -107,21 +107,31 @@ def test_rotation_is_block_diagonal_library_build(G, k):
                                rtol=1e-12, atol=1e-12)
 
 
-def test_rotation_g4096_one_hot_rows():
-    """For G = 4096 (dense R too big to test wholesale): rotating e_j gives row j of R."""
-    G = 4096
-    js = [0, 1, 3, 4095, 1234]
+@pytest.mark.parametrize("G", [4096, 16384, 65536])
+def test_rotation_large_g_one_hot_rows(G):
+    """For G = 4096 and up (dense R too big to test wholesale): rotating e_j gives
+    row j of R, the closed form read off the printed H4's sign pattern."""
+    n = int(round(np.log(G) / np.log(4)))
+    js = [0, 1, 3, G - 1, 1234, G // 2 + 77]
     X = np.zeros((len(js), G), np.float32)
     for r, j in enumerate(js):
         X[r, j] = 1.0
     rot = oracle.rotate_fast(X, G)
-    n = 6
     idx = np.arange(G)
     for r, j in enumerate(js):
         minus = np.zeros(G, np.int64)
         for p in range(n):
             minus += ((idx // 4**p) % 4 + (j // 4**p) % 4) == 3
         np.testing.assert_array_equal(rot[r], np.where(minus % 2, -1.0, 1.0) / 2.0**n)
+
+
+@pytest.mark.parametrize("G", [16384, 65536])
+def test_rotation_large_g_is_an_involution(G):
+    """R_G is symmetric and orthogonal, so rotating twice gives the input back."""
+    rng = np.random.default_rng(G)
+    X = rng.standard_normal((2, 2 * G)).astype(np.float32)
+    twice = oracle.rotate_fast(oracle.rotate_fast(X, G).astype(np.float32), G)
+    np.testing.assert_allclose(twice, X.astype(np.float64), rtol=0, atol=1e-5)
 
 
 @pytest.mark.parametrize("G", [4, 64, 256])
