@@ -32,10 +32,13 @@
 // share of K (so that about one CTA runs per SM).
 //   warp 0      TMA producer: 32-column fp32 slices of X (128 rows) and of
 //               A_ext's hi and lo rows, 128-byte swizzled, into a ring.
-//   warp 1      TMEM (r fp32 columns) and tcgen05.mma, M = 128, N = r, K = 8.
-//   warps 2-9   split each X slice in place: hi = the value with its low 13
-//               mantissa bits cleared, lo = value - hi into a second buffer
-//               with the same layout.
+//   warp 1      tcgen05.mma, M = 128, K = 8: the X operand from tensor
+//               memory, the A_ext slices from shared memory, fp32
+//               accumulators in tensor memory.
+//   warps 2-9   split each X slice, one row a thread: hi = the value with its
+//               low 13 mantissa bits cleared, lo = value - hi, both written
+//               to a tensor-memory ring (tcgen05.st), so that the MMAs read
+//               only A_ext from shared memory.
 //   then        each CTA's partial T goes to its shared memory; the cluster
 //               adds the partials in rank order (distributed shared memory),
 //               each CTA for its share of the rows, and writes T_ext.
@@ -59,6 +62,12 @@ constexpr int LD_THREADS = 64 + 32 * LD_SPLIT_WARPS;
 constexpr int LD_X_BYTES = LD_BM * LD_BK * 4;  // 16 KB
 constexpr int LD_SMEM_LIMIT = 227 * 1024;
 constexpr int LD_MAX_CLUSTER = 8;
+constexpr int LD_MAX_STAGES = 4;
+// tensor memory: the accumulators in columns [0, 256), the X ring in [256, 512),
+// one stage = hi (32 columns) then lo (32 columns)
+constexpr uint32_t LD_TMEM_COLS = 512;
+constexpr uint32_t LD_XRING_COL = 256;
+constexpr uint32_t LD_XRING_STAGE_COLS = 64;
 
 // kind::tf32: D fp32 (bit 4), A and B TF32 (format 2 at bits 7 and 10), both K-major, M = 128, N = n
 __host__ __device__ constexpr uint32_t tf32_idesc(int n)
@@ -66,13 +75,61 @@ __host__ __device__ constexpr uint32_t tf32_idesc(int n)
     return (1u << 4) | (2u << 7) | (2u << 10) | (uint32_t(n >> 3) << 17) | (uint32_t(LD_BM >> 4) << 24);
 }
 
-__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accumulate)
+// The X operand from tensor memory (M = 128 lanes, one TF32 element a column). The
+// accumulate flag is an immediate: a predicate computed at run time costs the issuing
+// thread about 20 cycles an instruction, and the loop below is bound by that thread.
+template <bool kAccumulate>
+__device__ __forceinline__ void mma_tf32_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc)
+{
+    if constexpr (kAccumulate)
+        asm volatile("tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, 1;" ::"r"(d_tmem), "r"(a_tmem),
+                     "l"(b), "r"(idesc)
+                     : "memory");
+    else
+        asm volatile("tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, 0;" ::"r"(d_tmem), "r"(a_tmem),
+                     "l"(b), "r"(idesc)
+                     : "memory");
+}
+
+// One 32-column slice: four K = 8 steps. kNacc == 3: Xh [Ah; Al] (N = 2 r) into columns
+// [0, 2r) and Xl Ah into [2r, 3r); kNacc == 1: the three products into one accumulator.
+// kFirst: the slice that starts the accumulators.
+template <int kNacc, bool kFirst>
+__device__ __forceinline__ void lora_slice_mma(uint32_t acc, uint32_t xh, uint64_t da, uint64_t dal, int r,
+                                               uint32_t idesc, uint32_t idesc2)
+{
+    const uint32_t xl = xh + 32u;
+#pragma unroll
+    for (int kk = 0; kk < LD_BK / 8; ++kk) {  // K = 8 TF32: 8 columns of X, 32 bytes of A
+        const uint32_t ax = xh + 8u * kk, al = xl + 8u * kk;
+        const uint64_t b = da + 2u * kk;
+        if constexpr (kNacc == 3) {
+            if (kFirst && kk == 0) {
+                mma_tf32_ta<false>(acc, ax, b, idesc2);
+                mma_tf32_ta<false>(acc + 2 * r, al, b, idesc);
+            } else {
+                mma_tf32_ta<true>(acc, ax, b, idesc2);
+                mma_tf32_ta<true>(acc + 2 * r, al, b, idesc);
+            }
+        } else {
+            if (kFirst && kk == 0)
+                mma_tf32_ta<false>(acc, ax, b, idesc);
+            else
+                mma_tf32_ta<true>(acc, ax, b, idesc);
+            mma_tf32_ta<true>(acc, ax, dal + 2u * kk, idesc);
+            mma_tf32_ta<true>(acc, al, b, idesc);
+        }
+    }
+}
+
+// 16 consecutive 32-bit columns of this thread's lane (warp-wide, 32 lanes)
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16])
 {
     asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+        "%14, %15, %16};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+        "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
         : "memory");
 }
 
@@ -89,12 +146,16 @@ __device__ __forceinline__ void cluster_sync()
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-__device__ __forceinline__ float ld_cluster_f32(uint32_t local_addr, uint32_t rank)
+// four floats at a 16-byte aligned address of the CTA of the given rank in this cluster
+__device__ __forceinline__ float4 ld_cluster_f32x4(uint32_t local_addr, uint32_t rank)
 {
     uint32_t a;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(local_addr), "r"(rank));
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(a)
+                 : "memory");
     return v;
 }
 
@@ -104,8 +165,7 @@ struct DownParams {
     int32_t kstages;      // ceil(k / 32), split over the cluster's CTAs
     int32_t stages;       // ring depth
     uint32_t a_bytes;     // r * 128: one slice of A (hi or lo)
-    uint32_t stage_bytes; // X hi + A hi + A lo + X lo
-    uint32_t tmem_cols;   // power of two >= max(32, r)
+    uint32_t stage_bytes; // X + A hi + A lo
     __nv_bfloat16 *t;     // T_ext [m, ldt]
     int64_t ldt;
     int32_t t_cols;       // columns of T_ext written: 3r, then zeros up to t_cols
@@ -133,6 +193,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b)
 // One CTA of a cluster: rows [128 * blockIdx.y, +128) of X, its share of the K
 // slices. The cluster's CTAs then add their partial T tiles (through
 // distributed shared memory, in rank order) and write T_ext.
+template <int kNacc>
 __global__ void __launch_bounds__(LD_THREADS, 1)
     lora_down_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmA, DownParams p)
 {
@@ -149,11 +210,11 @@ __global__ void __launch_bounds__(LD_THREADS, 1)
     const uint32_t done_bar = bars + 8u * (3 * S + 1);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + S * p.stage_bytes + 8 * (3 * S + 2));
     volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + S * p.stage_bytes + 8 * (3 * S + 2) + 4);
-    // stage s: [X hi | A hi | A lo | X lo]
+    // stage s: [X | A hi | A lo] in shared memory, [hi(X) | lo(X)] in the tensor-memory ring
     auto x_big = [&](int s) { return base + s * p.stage_bytes; };
     auto a_big = [&](int s) { return x_big(s) + LD_X_BYTES; };
     auto a_small = [&](int s) { return a_big(s) + p.a_bytes; };
-    auto x_small = [&](int s) { return a_small(s) + p.a_bytes; };
+    auto x_tmem = [&](int s) { return LD_XRING_COL + LD_XRING_STAGE_COLS * static_cast<uint32_t>(s); };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int row0 = static_cast<int>(blockIdx.y) * LD_BM;
@@ -179,7 +240,7 @@ __global__ void __launch_bounds__(LD_THREADS, 1)
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          static_cast<uint32_t>(__cvta_generic_to_shared(tmem_slot))),
-                     "r"(p.tmem_cols)
+                     "r"(LD_TMEM_COLS)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
@@ -197,9 +258,9 @@ __global__ void __launch_bounds__(LD_THREADS, 1)
         if (lane == 0) {
             int issued = 0;
             bool ok = true;
+            int s = 0;
+            uint32_t ph = 0;
             for (int i = 0; i < nks; ++i) {
-                const int s = i % S;
-                const uint32_t ph = static_cast<uint32_t>(i / S) & 1u;
                 if (*abort_flag || !mbar_wait(empty_bar(s), ph ^ 1u)) {
                     ok = false;
                     break;
@@ -210,6 +271,10 @@ __global__ void __launch_bounds__(LD_THREADS, 1)
                 tma_load_2d(a_big(s), &tmA, kx, 0, full_bar(s));       // rows 0..r-1: hi(A)
                 tma_load_2d(a_small(s), &tmA, kx, p.r, full_bar(s));   // rows r..2r-1: lo(A)
                 ++issued;
+                if (++s == S) {
+                    s = 0;
+                    ph ^= 1u;
+                }
             }
             if (!ok) {
                 fail();
@@ -221,25 +286,46 @@ __global__ void __launch_bounds__(LD_THREADS, 1)
         __syncwarp();
     } else if (warp == 1) {
         if (lane == 0) {
-            const uint32_t idesc = tf32_idesc(p.r);
+            const uint32_t idesc = tf32_idesc(p.r), idesc2 = tf32_idesc(kNacc == 3 ? 2 * p.r : p.r);
+            // This thread bounds the loop: the MMAs of a slice take about 400 cycles, and any
+            // shared-memory access this thread makes after issuing them (a barrier wait, a flag
+            // read) returns only once they have all entered the tensor pipe, which then runs dry
+            // until the next MMAs come. So where the ring holds three slices or more, the thread
+            // waits for two at a time and issues both back to back: one such gap every two
+            // slices. (With two, the producer could not refill while both are in use.) No
+            // division, and one descriptor add a slice.
+            const uint64_t da0 = smem_desc(a_big(0));
+            const uint64_t dstep = p.stage_bytes >> 4, dlo = p.a_bytes >> 4;
+            uint64_t da = da0;
             bool ok = true;
-            for (int i = 0; i < nks; ++i) {
-                const int s = i % S;
-                const uint32_t ph = static_cast<uint32_t>(i / S) & 1u;
-                if (*abort_flag || !mbar_wait(conv_bar(s), ph)) {
+            int s = 0;
+            uint32_t ph = 0;
+            for (int i = 0; i < nks;) {
+                const bool pair = S >= 3 && i + 1 < nks;
+                const int s1 = s + 1 == S ? 0 : s + 1;
+                const uint32_t ph1 = s + 1 == S ? ph ^ 1u : ph;
+                if (!mbar_wait(conv_bar(s), ph) || (pair && !mbar_wait(conv_bar(s1), ph1)) || *abort_flag) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < LD_BK / 8; ++kk) {  // K = 8 TF32 = 32 bytes per instruction
-                    const uint64_t xh = smem_desc(x_big(s)) + 2u * kk, ah = smem_desc(a_big(s)) + 2u * kk;
-                    const uint64_t xl = smem_desc(x_small(s)) + 2u * kk, al = smem_desc(a_small(s)) + 2u * kk;
-                    mma_tf32(tmem_base, xh, ah, idesc, (i > 0 || kk > 0) ? 1u : 0u);
-                    mma_tf32(tmem_base, xh, al, idesc, 1u);
-                    mma_tf32(tmem_base, xl, ah, idesc, 1u);
-                }
+                if (i == 0)
+                    lora_slice_mma<kNacc, true>(tmem_base, tmem_base + x_tmem(s), da, da + dlo, p.r, idesc, idesc2);
+                else
+                    lora_slice_mma<kNacc, false>(tmem_base, tmem_base + x_tmem(s), da, da + dlo, p.r, idesc, idesc2);
                 mma_commit(empty_bar(s));
+                da = s1 == 0 ? da0 : da + dstep;
+                s = s1;
+                ph = ph1;
+                if (pair) {
+                    lora_slice_mma<kNacc, false>(tmem_base, tmem_base + x_tmem(s), da, da + dlo, p.r, idesc, idesc2);
+                    mma_commit(empty_bar(s));
+                    const int s2 = s + 1 == S ? 0 : s + 1;
+                    if (s2 == 0) ph ^= 1u;
+                    da = s2 == 0 ? da0 : da + dstep;
+                    s = s2;
+                }
+                i += pair ? 2 : 1;
             }
             if (!ok) fail();
             mma_commit(accf_bar);  // after every MMA issued above
@@ -248,50 +334,88 @@ __global__ void __launch_bounds__(LD_THREADS, 1)
         }
         __syncwarp();
     } else {
-        const int tid = threadIdx.x - 64;  // 0..255
+        // a warp reaches only its TMEM lane quadrant (warp % 4): two warps a quadrant, one for
+        // columns 0-15 of the slice, one for 16-31; a thread takes one row of X
+        const int q = warp & 3, half = (warp - 2) >> 2;
+        const int row = q * 32 + lane;
         bool ok = true;
+        int s = 0;
+        uint32_t ph = 0;
         for (int i = 0; i < nks; ++i) {
-            const int s = i % S;
-            const uint32_t ph = static_cast<uint32_t>(i / S) & 1u;
             if (*abort_flag || !mbar_wait(full_bar(s), ph)) {
                 ok = false;
                 break;
             }
-            // the split is elementwise, so the swizzled layout does not matter: same offset in both buffers
-            float4 *xb = reinterpret_cast<float4 *>(gbase + (x_big(s) - base));
-            float4 *xs = reinterpret_cast<float4 *>(gbase + (x_small(s) - base));
+            // the TMEM stage was last read by the MMAs of slice i - S, which completed before the
+            // producer refilled this stage
+            tc_fence_after();
+            // 128-byte swizzle: 16-byte chunk c of a row sits at chunk c ^ (row % 8), so the eight
+            // rows of a lane octet read eight distinct bank groups
+            const uint8_t *xrow = gbase + (x_big(s) - base) + row * 128;
+            uint32_t hi[16], lo[16];
 #pragma unroll
-            for (int j = 0; j < LD_X_BYTES / 16 / (32 * LD_SPLIT_WARPS); ++j) {
-                float4 v = xb[tid + 32 * LD_SPLIT_WARPS * j], l;
+            for (int j = 0; j < 4; ++j) {
+                const int c = half * 4 + j;
+                float4 v = *reinterpret_cast<const float4 *>(xrow + ((c ^ (row & 7)) << 4)), l;
                 split_tf32(v, l);
-                xb[tid + 32 * LD_SPLIT_WARPS * j] = v;
-                xs[tid + 32 * LD_SPLIT_WARPS * j] = l;
+                hi[4 * j] = __float_as_uint(v.x);
+                hi[4 * j + 1] = __float_as_uint(v.y);
+                hi[4 * j + 2] = __float_as_uint(v.z);
+                hi[4 * j + 3] = __float_as_uint(v.w);
+                lo[4 * j] = __float_as_uint(l.x);
+                lo[4 * j + 1] = __float_as_uint(l.y);
+                lo[4 * j + 2] = __float_as_uint(l.z);
+                lo[4 * j + 3] = __float_as_uint(l.w);
             }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the tensor core
+            const uint32_t ta = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + x_tmem(s) + 16u * half;
+            tmem_st16(ta, hi);
+            tmem_st16(ta + 32u, lo);
+            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(conv_bar(s));
+            if (++s == S) {
+                s = 0;
+                ph ^= 1u;
+            }
         }
         if (!ok) fail();
     }
 
-    // partial T (this CTA's K share) from tensor memory to shared memory, [128][r + 1] fp32
+    // partial T (this CTA's K share) from tensor memory to shared memory, [128][r + 4] fp32
     const int r = p.r;
-    const int pitch = r + 1;  // odd: row-per-lane writes and column reads are conflict-free
+    // r + 4 with r % 16 == 0: rows start 16-byte aligned, and a lane octet's float4 stores (one
+    // row a lane) fall in eight distinct 16-byte bank groups
+    const int pitch = r + 4;
     float *part = reinterpret_cast<float *>(gbase);
     const uint32_t part_addr = base;
     bool ok = true;
-    if (warp >= 2 && warp < 6) {  // four warps, one per TMEM lane quadrant
+    if (warp >= 2) {  // eight warps: two a TMEM lane quadrant, alternate 32-column blocks
         ok = mbar_wait(accf_bar, 0) && !*abort_flag;
         if (ok) {
             tc_fence_after();
-            const int q = warp & 3;
+            const int q = warp & 3, half = (warp - 2) >> 2;
             float *dst = part + (q * 32 + lane) * pitch;
-            for (int c0 = 0; c0 < r; c0 += 32) {
+            for (int c0 = 32 * half; c0 < r; c0 += 64) {
+                const uint32_t ta = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + c0;
                 uint32_t v[32];
-                tmem_ld32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + c0, v);
+                float t[32];
+                tmem_ld32(ta, v);
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    if (c0 + j < r) dst[c0 + j] = __uint_as_float(v[j]);
+                for (int j = 0; j < 32; ++j) t[j] = __uint_as_float(v[j]);
+                if constexpr (kNacc == 3) {  // the accumulators added in a fixed order
+#pragma unroll
+                    for (int a = 1; a < 3; ++a) {
+                        tmem_ld32(ta + a * r, v);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) t[j] += __uint_as_float(v[j]);
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j)  // r % 16 == 0: a quad is wholly in or out
+                    if (c0 + 4 * j < r)
+                        *reinterpret_cast<float4 *>(dst + c0 + 4 * j) =
+                            make_float4(t[4 * j], t[4 * j + 1], t[4 * j + 2], t[4 * j + 3]);
             }
         } else {
             fail();
@@ -299,53 +423,69 @@ __global__ void __launch_bounds__(LD_THREADS, 1)
     }
     tc_fence_before();
     cluster_sync();  // every CTA's partial is in its shared memory (all CTAs reach this)
-    // this CTA adds the cluster's partials, in rank order, for its share of the rows
+    const int rows_per = (LD_BM + csize - 1) / csize;  // rows [rb, re) are this CTA's to add up and write
+    const int rb = static_cast<int>(rank) * rows_per;
+    const int re = rb + rows_per < LD_BM ? rb + rows_per : LD_BM;
+    // this CTA adds the cluster's partials, in rank order, for its rows: four columns a thread,
+    // two such quads in flight so that all their remote loads overlap
     if (!*abort_flag) {
-        const int rows_per = (LD_BM + csize - 1) / csize;
-        const int rb = static_cast<int>(rank) * rows_per;
-        const int re = rb + rows_per < LD_BM ? rb + rows_per : LD_BM;
-        const int pairs = r / 2;
-        for (int idx = threadIdx.x; idx < (re - rb) * pairs; idx += LD_THREADS) {
-            const int rr = rb + idx / pairs, c = (idx % pairs) * 2;
-            const uint32_t a = part_addr + static_cast<uint32_t>((rr * pitch + c) * 4);
-            // all the remote loads first (they overlap), then the sums in rank order
-            float v0[LD_MAX_CLUSTER], v1[LD_MAX_CLUSTER];
+        const int quads = r / 4;
+        const int n = re > rb ? (re - rb) * quads : 0;
+        for (int i0 = threadIdx.x; i0 < n; i0 += 2 * LD_THREADS) {
+            float4 v[2][LD_MAX_CLUSTER];
 #pragma unroll
-            for (int src = 0; src < LD_MAX_CLUSTER; ++src) {
-                if (src < csize) {
-                    v0[src] = ld_cluster_f32(a, static_cast<uint32_t>(src));
-                    v1[src] = ld_cluster_f32(a + 4, static_cast<uint32_t>(src));
+            for (int u = 0; u < 2; ++u) {
+                const int idx = i0 + u * LD_THREADS;
+                if (idx < n) {
+                    const int rr = rb + idx / quads, c = (idx % quads) * 4;
+                    const uint32_t a = part_addr + static_cast<uint32_t>((rr * pitch + c) * 4);
+#pragma unroll
+                    for (int src = 0; src < LD_MAX_CLUSTER; ++src)
+                        if (src < csize) v[u][src] = ld_cluster_f32x4(a, static_cast<uint32_t>(src));
                 }
             }
-            float t0 = 0.0f, t1 = 0.0f;
 #pragma unroll
-            for (int src = 0; src < LD_MAX_CLUSTER; ++src) {
-                if (src < csize) {
-                    t0 += v0[src];
-                    t1 += v1[src];
+            for (int u = 0; u < 2; ++u) {
+                const int idx = i0 + u * LD_THREADS;
+                if (idx >= n) continue;
+                const int rr = rb + idx / quads, c = (idx % quads) * 4;
+                const int64_t row = static_cast<int64_t>(row0) + rr;
+                if (row >= p.m) continue;
+                float4 t = v[u][0];
+#pragma unroll
+                for (int src = 1; src < LD_MAX_CLUSTER; ++src) {
+                    if (src < csize) {
+                        t.x += v[u][src].x;
+                        t.y += v[u][src].y;
+                        t.z += v[u][src].z;
+                        t.w += v[u][src].w;
+                    }
                 }
+                const __nv_bfloat162 h01 = __floats2bfloat162_rn(t.x, t.y), h23 = __floats2bfloat162_rn(t.z, t.w);
+                const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
+                uint2 hi, lo;
+                hi.x = *reinterpret_cast<const uint32_t *>(&h01);
+                hi.y = *reinterpret_cast<const uint32_t *>(&h23);
+                lo.x = pack_bf16x2(t.x - f01.x, t.y - f01.y);
+                lo.y = pack_bf16x2(t.z - f23.x, t.w - f23.y);
+                // T_ext is 16-byte aligned with ldt % 8 == 0, and c, r are multiples of 4: 8-byte stores
+                __nv_bfloat16 *dst = p.t + row * p.ldt;
+                *reinterpret_cast<uint2 *>(dst + c) = hi;
+                *reinterpret_cast<uint2 *>(dst + r + c) = hi;
+                *reinterpret_cast<uint2 *>(dst + 2 * r + c) = lo;
             }
-            const int64_t row = static_cast<int64_t>(row0) + rr;
-            if (row >= p.m) continue;
-            const __nv_bfloat162 h = __floats2bfloat162_rn(t0, t1);
-            const float2 hf = __bfloat1622float2(h);
-            uint32_t *dst = reinterpret_cast<uint32_t *>(p.t + row * p.ldt);
-            const uint32_t hb = *reinterpret_cast<const uint32_t *>(&h);
-            dst[c / 2] = hb;
-            dst[(r + c) / 2] = hb;
-            dst[(2 * r + c) / 2] = pack_bf16x2(t0 - hf.x, t1 - hf.y);
         }
-        // the zero columns past 3 r
-        const int zpairs = (p.t_cols - 3 * r) / 2;
-        for (int idx = threadIdx.x; idx < (re - rb) * zpairs; idx += LD_THREADS) {
-            const int64_t row = static_cast<int64_t>(row0) + rb + idx / zpairs;
+        // the zero columns past 3 r (a multiple of 16 of them)
+        const int zquads = (p.t_cols - 3 * r) / 4;
+        for (int idx = threadIdx.x; idx < (re - rb) * zquads; idx += LD_THREADS) {
+            const int64_t row = static_cast<int64_t>(row0) + rb + idx / zquads;
             if (row < p.m)
-                reinterpret_cast<uint32_t *>(p.t + row * p.ldt)[(3 * r) / 2 + idx % zpairs] = 0u;
+                *reinterpret_cast<uint2 *>(p.t + row * p.ldt + 3 * r + 4 * (idx % zquads)) = make_uint2(0u, 0u);
         }
     }
     cluster_sync();  // no CTA leaves while another may still read its partial
     if (warp == 1)
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(p.tmem_cols)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(LD_TMEM_COLS)
                      : "memory");
 }
 
@@ -429,24 +569,23 @@ cudaError_t launch_lora_down(const float *X, int64_t m, int32_t k, int64_t ldx, 
     p.r = r;
     p.kstages = (k + LD_BK - 1) / LD_BK;
     p.a_bytes = static_cast<uint32_t>(r) * LD_BK * 4;
-    p.stage_bytes = 2u * (LD_X_BYTES + p.a_bytes);
+    p.stage_bytes = LD_X_BYTES + 2u * p.a_bytes;
     const int fixed = 1024 + 256;  // alignment slack, barriers, TMEM slot and flag
     int stages = (LD_SMEM_LIMIT - fixed) / static_cast<int>(p.stage_bytes);
-    stages = stages > 4 ? 4 : stages;
+    stages = stages > LD_MAX_STAGES ? LD_MAX_STAGES : stages;  // the TMEM ring has four
     if (stages < 2) return cudaErrorInvalidValue;
-    // the partial-T tile [128][r + 1] fp32 reuses the ring once the K loop is done
-    if (static_cast<int64_t>(LD_BM) * (r + 1) * 4 > static_cast<int64_t>(stages) * p.stage_bytes)
+    // the partial-T tile [128][r + 4] fp32 reuses the ring once the K loop is done
+    if (static_cast<int64_t>(LD_BM) * (r + 4) * 4 > static_cast<int64_t>(stages) * p.stage_bytes)
         return cudaErrorInvalidValue;
     p.stages = stages;
-    uint32_t cols = 32;
-    while (cols < static_cast<uint32_t>(r)) cols <<= 1;
-    p.tmem_cols = cols;
+    // three accumulators where 3 r columns fit below the X ring, else one
+    auto kernel = 3 * r <= static_cast<int>(LD_XRING_COL) ? lora_down_kernel<3> : lora_down_kernel<1>;
     p.t = static_cast<__nv_bfloat16 *>(t);
     p.ldt = ldt;
     p.t_cols = lora_cols(r);
     p.dev_status = dev_status;
     const int smem = fixed + stages * static_cast<int>(p.stage_bytes);
-    cudaError_t e = cudaFuncSetAttribute(lora_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const int64_t row_blocks = (m + LD_BM - 1) / LD_BM;
     if (row_blocks > 65535) return cudaErrorInvalidConfiguration;
@@ -468,7 +607,7 @@ cudaError_t launch_lora_down(const float *X, int64_t m, int32_t k, int64_t ldx, 
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, lora_down_kernel, mx, ma, p);
+    e = cudaLaunchKernelEx(&cfg, kernel, mx, ma, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
