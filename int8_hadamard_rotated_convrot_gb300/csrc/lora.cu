@@ -32,13 +32,14 @@
 // share of K (so that about one CTA runs per SM).
 //   warp 0      TMA producer: 32-column fp32 slices of X (128 rows) and of
 //               A_ext's hi and lo rows, 128-byte swizzled, into a ring.
-//   warp 1      tcgen05.mma, M = 128, K = 8: the X operand from tensor
-//               memory, the A_ext slices from shared memory, fp32
-//               accumulators in tensor memory.
+//   warp 1      tcgen05.mma, M = 128, K = 8: the A_ext slices from shared
+//               memory, fp32 accumulators in tensor memory; lo(X) from a
+//               tensor-memory ring, hi(X) from the X slice itself (its TF32
+//               view) up to N = 128 an MMA, else from the ring too.
 //   warps 2-9   split each X slice, one row a thread: hi = the value with its
-//               low 13 mantissa bits cleared, lo = value - hi, both written
-//               to a tensor-memory ring (tcgen05.st), so that the MMAs read
-//               only A_ext from shared memory.
+//               low 13 mantissa bits cleared, lo = value - hi, written to
+//               the tensor-memory ring with tcgen05.st (hi only where the
+//               MMAs take it from there).
 //   then        each CTA's partial T goes to its shared memory; the cluster
 //               adds the partials in rank order (distributed shared memory),
 //               each CTA for its share of the rows, and writes T_ext.
@@ -91,33 +92,60 @@ __device__ __forceinline__ void mma_tf32_ta(uint32_t d_tmem, uint32_t a_tmem, ui
                      : "memory");
 }
 
+// The X operand from shared memory (the TMA'd slice, K-major, 128-byte swizzle). As a TF32
+// operand the tensor core reads an fp32 value's sign, exponent and top 10 mantissa bits, so
+// the raw slice serves as hi(X).
+template <bool kAccumulate>
+__device__ __forceinline__ void mma_tf32_sa(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc)
+{
+    if constexpr (kAccumulate)
+        asm volatile("tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, 1;" ::"r"(d_tmem), "l"(a), "l"(b),
+                     "r"(idesc)
+                     : "memory");
+    else
+        asm volatile("tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, 0;" ::"r"(d_tmem), "l"(a), "l"(b),
+                     "r"(idesc)
+                     : "memory");
+}
+
+// hi(X) as the A operand: the raw slice in shared memory (kXhSmem), or the TMEM ring's hi columns
+template <bool kXhSmem, bool kAccumulate>
+__device__ __forceinline__ void mma_xh(uint32_t d_tmem, uint64_t x_desc, uint32_t x_tmem, uint64_t b, uint32_t idesc)
+{
+    if constexpr (kXhSmem)
+        mma_tf32_sa<kAccumulate>(d_tmem, x_desc, b, idesc);
+    else
+        mma_tf32_ta<kAccumulate>(d_tmem, x_tmem, b, idesc);
+}
+
 // One 32-column slice: four K = 8 steps. kNacc == 3: Xh [Ah; Al] (N = 2 r) into columns
 // [0, 2r) and Xl Ah into [2r, 3r); kNacc == 1: the three products into one accumulator.
-// kFirst: the slice that starts the accumulators.
-template <int kNacc, bool kFirst>
-__device__ __forceinline__ void lora_slice_mma(uint32_t acc, uint32_t xh, uint64_t da, uint64_t dal, int r,
-                                               uint32_t idesc, uint32_t idesc2)
+// lo(X) always comes from the TMEM ring (columns xt + 32 ...); hi(X) from the X slice in shared
+// memory (descriptor dx) when kXhSmem, else from the ring (columns xt ...). kFirst: the slice
+// that starts the accumulators.
+template <int kNacc, bool kXhSmem, bool kFirst>
+__device__ __forceinline__ void lora_slice_mma(uint32_t acc, uint32_t xt, uint64_t dx, uint64_t da, uint64_t dal,
+                                               int r, uint32_t idesc, uint32_t idesc2)
 {
-    const uint32_t xl = xh + 32u;
 #pragma unroll
-    for (int kk = 0; kk < LD_BK / 8; ++kk) {  // K = 8 TF32: 8 columns of X, 32 bytes of A
-        const uint32_t ax = xh + 8u * kk, al = xl + 8u * kk;
-        const uint64_t b = da + 2u * kk;
+    for (int kk = 0; kk < LD_BK / 8; ++kk) {  // K = 8 TF32: 8 columns of X, 32 bytes of X or A a row
+        const uint32_t ht = xt + 8u * kk, lt = xt + 32u + 8u * kk;
+        const uint64_t hd = dx + 2u * kk, b = da + 2u * kk;
         if constexpr (kNacc == 3) {
             if (kFirst && kk == 0) {
-                mma_tf32_ta<false>(acc, ax, b, idesc2);
-                mma_tf32_ta<false>(acc + 2 * r, al, b, idesc);
+                mma_xh<kXhSmem, false>(acc, hd, ht, b, idesc2);
+                mma_tf32_ta<false>(acc + 2 * r, lt, b, idesc);
             } else {
-                mma_tf32_ta<true>(acc, ax, b, idesc2);
-                mma_tf32_ta<true>(acc + 2 * r, al, b, idesc);
+                mma_xh<kXhSmem, true>(acc, hd, ht, b, idesc2);
+                mma_tf32_ta<true>(acc + 2 * r, lt, b, idesc);
             }
         } else {
             if (kFirst && kk == 0)
-                mma_tf32_ta<false>(acc, ax, b, idesc);
+                mma_xh<kXhSmem, false>(acc, hd, ht, b, idesc);
             else
-                mma_tf32_ta<true>(acc, ax, b, idesc);
-            mma_tf32_ta<true>(acc, ax, dal + 2u * kk, idesc);
-            mma_tf32_ta<true>(acc, al, b, idesc);
+                mma_xh<kXhSmem, true>(acc, hd, ht, b, idesc);
+            mma_xh<kXhSmem, true>(acc, hd, ht, dal + 2u * kk, idesc);
+            mma_tf32_ta<true>(acc, lt, b, idesc);
         }
     }
 }
@@ -193,7 +221,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b)
 // One CTA of a cluster: rows [128 * blockIdx.y, +128) of X, its share of the K
 // slices. The cluster's CTAs then add their partial T tiles (through
 // distributed shared memory, in rank order) and write T_ext.
-template <int kNacc>
+template <int kNacc, bool kXhSmem>
 __global__ void __launch_bounds__(LD_THREADS, 1)
     lora_down_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmA, DownParams p)
 {
@@ -295,7 +323,7 @@ __global__ void __launch_bounds__(LD_THREADS, 1)
             // slices. (With two, the producer could not refill while both are in use.) No
             // division, and one descriptor add a slice.
             const uint64_t da0 = smem_desc(a_big(0));
-            const uint64_t dstep = p.stage_bytes >> 4, dlo = p.a_bytes >> 4;
+            const uint64_t dstep = p.stage_bytes >> 4, dlo = p.a_bytes >> 4, dx_off = LD_X_BYTES >> 4;
             uint64_t da = da0;
             bool ok = true;
             int s = 0;
@@ -310,15 +338,18 @@ __global__ void __launch_bounds__(LD_THREADS, 1)
                 }
                 tc_fence_after();
                 if (i == 0)
-                    lora_slice_mma<kNacc, true>(tmem_base, tmem_base + x_tmem(s), da, da + dlo, p.r, idesc, idesc2);
+                    lora_slice_mma<kNacc, kXhSmem, true>(tmem_base, tmem_base + x_tmem(s), da - dx_off, da, da + dlo,
+                                                         p.r, idesc, idesc2);
                 else
-                    lora_slice_mma<kNacc, false>(tmem_base, tmem_base + x_tmem(s), da, da + dlo, p.r, idesc, idesc2);
+                    lora_slice_mma<kNacc, kXhSmem, false>(tmem_base, tmem_base + x_tmem(s), da - dx_off, da, da + dlo,
+                                                          p.r, idesc, idesc2);
                 mma_commit(empty_bar(s));
                 da = s1 == 0 ? da0 : da + dstep;
                 s = s1;
                 ph = ph1;
                 if (pair) {
-                    lora_slice_mma<kNacc, false>(tmem_base, tmem_base + x_tmem(s), da, da + dlo, p.r, idesc, idesc2);
+                    lora_slice_mma<kNacc, kXhSmem, false>(tmem_base, tmem_base + x_tmem(s), da - dx_off, da, da + dlo,
+                                                          p.r, idesc, idesc2);
                     mma_commit(empty_bar(s));
                     const int s2 = s + 1 == S ? 0 : s + 1;
                     if (s2 == 0) ph ^= 1u;
@@ -368,7 +399,7 @@ __global__ void __launch_bounds__(LD_THREADS, 1)
                 lo[4 * j + 3] = __float_as_uint(l.w);
             }
             const uint32_t ta = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + x_tmem(s) + 16u * half;
-            tmem_st16(ta, hi);
+            if constexpr (!kXhSmem) tmem_st16(ta, hi);
             tmem_st16(ta + 32u, lo);
             asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             tc_fence_before();
@@ -578,8 +609,12 @@ cudaError_t launch_lora_down(const float *X, int64_t m, int32_t k, int64_t ldx, 
     if (static_cast<int64_t>(LD_BM) * (r + 4) * 4 > static_cast<int64_t>(stages) * p.stage_bytes)
         return cudaErrorInvalidValue;
     p.stages = stages;
-    // three accumulators where 3 r columns fit below the X ring, else one
-    auto kernel = 3 * r <= static_cast<int>(LD_XRING_COL) ? lora_down_kernel<3> : lora_down_kernel<1>;
+    // three accumulators where 3 r columns fit below the X ring, else one; hi(X) read from the X
+    // slice in shared memory up to N = 128 an MMA (beyond, those reads bound the loop and the
+    // TMEM copy is faster: r = 256 34.6 against 32.9 us, r = 64 17.5 against 18.4)
+    auto kernel = 3 * r <= static_cast<int>(LD_XRING_COL) ? lora_down_kernel<3, true>
+                  : r <= 128                              ? lora_down_kernel<1, true>
+                                                          : lora_down_kernel<1, false>;
     p.t = static_cast<__nv_bfloat16 *>(t);
     p.ldt = ldt;
     p.t_cols = lora_cols(r);
