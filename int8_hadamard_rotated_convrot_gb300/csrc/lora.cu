@@ -63,9 +63,10 @@ constexpr int LD_THREADS = 64 + 32 * LD_SPLIT_WARPS;
 constexpr int LD_X_BYTES = LD_BM * LD_BK * 4;  // 16 KB
 constexpr int LD_SMEM_LIMIT = 227 * 1024;
 constexpr int LD_MAX_CLUSTER = 8;
-constexpr int LD_MAX_STAGES = 4;
-// tensor memory: the accumulators in columns [0, 256), the X ring in [256, 512),
-// one stage = hi (32 columns) then lo (32 columns)
+// tensor memory: the accumulators in columns [0, 256), the X ring in [256, 512): a stage is
+// lo(X) alone (32 columns) where the MMAs read hi(X) from shared memory, else hi then lo (64)
+constexpr int LD_MAX_STAGES = 4;     // hi and lo in the ring
+constexpr int LD_MAX_STAGES_LO = 6;  // lo alone (up to eight fit; shared memory holds six)
 constexpr uint32_t LD_TMEM_COLS = 512;
 constexpr uint32_t LD_XRING_COL = 256;
 constexpr uint32_t LD_XRING_STAGE_COLS = 64;
@@ -242,7 +243,11 @@ __global__ void __launch_bounds__(LD_THREADS, 1)
     auto x_big = [&](int s) { return base + s * p.stage_bytes; };
     auto a_big = [&](int s) { return x_big(s) + LD_X_BYTES; };
     auto a_small = [&](int s) { return a_big(s) + p.a_bytes; };
-    auto x_tmem = [&](int s) { return LD_XRING_COL + LD_XRING_STAGE_COLS * static_cast<uint32_t>(s); };
+    // the column of slice s's hi(X) (lo(X) is 32 further on); with kXhSmem only lo is stored
+    auto x_tmem = [&](int s) {
+        return kXhSmem ? LD_XRING_COL - 32u + 32u * static_cast<uint32_t>(s)
+                       : LD_XRING_COL + LD_XRING_STAGE_COLS * static_cast<uint32_t>(s);
+    };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int row0 = static_cast<int>(blockIdx.y) * LD_BM;
@@ -601,9 +606,11 @@ cudaError_t launch_lora_down(const float *X, int64_t m, int32_t k, int64_t ldx, 
     p.kstages = (k + LD_BK - 1) / LD_BK;
     p.a_bytes = static_cast<uint32_t>(r) * LD_BK * 4;
     p.stage_bytes = LD_X_BYTES + 2u * p.a_bytes;
+    const bool xh_smem = r <= 128;  // hi(X) read from the X slice (see below)
     const int fixed = 1024 + 256;  // alignment slack, barriers, TMEM slot and flag
     int stages = (LD_SMEM_LIMIT - fixed) / static_cast<int>(p.stage_bytes);
-    stages = stages > LD_MAX_STAGES ? LD_MAX_STAGES : stages;  // the TMEM ring has four
+    const int max_stages = xh_smem ? LD_MAX_STAGES_LO : LD_MAX_STAGES;  // what the TMEM ring holds
+    stages = stages > max_stages ? max_stages : stages;
     if (stages < 2) return cudaErrorInvalidValue;
     // the partial-T tile [128][r + 4] fp32 reuses the ring once the K loop is done
     if (static_cast<int64_t>(LD_BM) * (r + 4) * 4 > static_cast<int64_t>(stages) * p.stage_bytes)
@@ -613,7 +620,7 @@ cudaError_t launch_lora_down(const float *X, int64_t m, int32_t k, int64_t ldx, 
     // slice in shared memory up to N = 128 an MMA (beyond, those reads bound the loop and the
     // TMEM copy is faster: r = 256 34.6 against 32.9 us, r = 64 17.5 against 18.4)
     auto kernel = 3 * r <= static_cast<int>(LD_XRING_COL) ? lora_down_kernel<3, true>
-                  : r <= 128                              ? lora_down_kernel<1, true>
+                  : xh_smem                               ? lora_down_kernel<1, true>
                                                           : lora_down_kernel<1, false>;
     p.t = static_cast<__nv_bfloat16 *>(t);
     p.ldt = ldt;
