@@ -323,10 +323,10 @@ def run_ours(args):
                     pxs[0][j], pws[0][j], biases[0], st.act, wl.G, codes, out=pxs[1][j], work=works[j],
                     stream=stream)))
             elif wl.lora_r and s_i == 0:
-                # the pack reads X row by row first; T = X A^T then takes its 128-byte slices of
-                # those rows from L2
-                ops.append(("pack", pack))
+                # T = X A^T first: the pack then finds X in L2 (it reads X with an evict-first
+                # hint, so X would not wait in L2 for lora_down the other way round)
                 ops.append(("lora_down", lambda h=h: cr.convrot_lora_down(h, A_l, out=T_ext[j], stream=stream)))
+                ops.append(("pack", pack))
                 ops.append(("gemm", lambda s_i=s_i, st=st: cr.convrot_linear_lora(
                     pxs[s_i][j], pws[s_i][j], biases[s_i], st.act, T_ext[j], B_ext, wl.lora_r, out=Ys[s_i][j],
                     stream=stream)))

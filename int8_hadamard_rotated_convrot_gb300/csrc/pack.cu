@@ -793,11 +793,28 @@ __global__ void __launch_bounds__(512) __maxnreg__(kLayout == 2 ? 80 : 128) pack
         asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
                      "r"(static_cast<uint32_t>(nr) * P.row_bytes)
                      : "memory");
-        for (int i = 0; i < nr; ++i)
-            asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                             ring_base + stage * P.stage_bytes + i * P.row_bytes),
-                         "l"(a.x + (r0 + i) * a.ldx), "r"(P.row_bytes), "r"(bar)
-                         : "memory");
+        if (NS == 1) {
+            // X is read once: its lines go first when L2 needs room, so that what the next
+            // kernel reads (the weights and these codes) stays. Measured on the short-row form
+            // (one stage, five CTAs an SM; K = 3072): the pack 16.5 -> 16.0 us, G = 4 14.6 ->
+            // 14.2, G = 1024 18.1 -> 17.4, the q/k/v step 152-155 -> 149-151 us, MLP up
+            // unchanged. On the two-stage form (MLP down, K = 12288) it cost 49.3 -> 51.4 us,
+            // so the other forms read X without the hint.
+            uint64_t policy;
+            asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
+            for (int i = 0; i < nr; ++i)
+                asm volatile(
+                    "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, "
+                    "[%3], %4;" ::"r"(ring_base + stage * P.stage_bytes + i * P.row_bytes),
+                    "l"(a.x + (r0 + i) * a.ldx), "r"(P.row_bytes), "r"(bar), "l"(policy)
+                    : "memory");
+        } else {
+            for (int i = 0; i < nr; ++i)
+                asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                                 ring_base + stage * P.stage_bytes + i * P.row_bytes),
+                             "l"(a.x + (r0 + i) * a.ldx), "r"(P.row_bytes), "r"(bar)
+                             : "memory");
+        }
     };
 
     if (threadIdx.x == 0)
