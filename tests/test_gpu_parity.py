@@ -682,7 +682,8 @@ def test_graph_replay_equals_eager_steps():
 
 # ---- runtime LoRA side branch
 
-@pytest.mark.parametrize("m,k,r", [(300, 512, 16), (129, 3072, 64), (64, 200, 48), (1000, 1024, 256)])
+@pytest.mark.parametrize("m,k,r", [(300, 512, 16), (129, 3072, 64), (64, 200, 48), (1000, 1024, 256),
+                                   (200, 1000, 96), (384, 2048, 176)])
 def test_lora_down_against_oracle(m, k, r):
     """T = X A^T (three-term TF32 on tcgen05), stored as [hi | hi | lo | 0]."""
     rng = np.random.default_rng(m + k + r)
