@@ -216,6 +216,24 @@ def test_empty_pack_and_linear():
     assert Y.shape == (0, 8)
 
 
+def test_empty_lora_and_fused_pack():
+    """m == 0 is a no-op for the LoRA calls and the fused linear + pack as well."""
+    X = torch.empty((0, 256), dtype=torch.float32, device="cuda")
+    p = cr.convrot_pack_activations(X, 256, cr.CODES_BF16)  # (the LoRA chunk runs with bf16 codes)
+    w = cr.convrot_quantize_weights(torch.randn(256, 256, device="cuda"), 256, cr.CODES_BF16)
+    A_ext = cr.convrot_lora_prepare_down(0.05 * torch.randn(16, 256, device="cuda"))
+    T = cr.convrot_lora_down(X, A_ext)
+    assert T.shape == (0, cr.lora_cols(16))
+    B_ext = cr.convrot_lora_prepare(0.02 * torch.randn(256, 16, device="cuda"), 2.0)
+    Y = cr.convrot_linear_lora(p, w, None, cr.ACT_NONE, T, B_ext, 16)
+    assert Y.shape == (0, 256)
+    Y2 = cr.convrot_linear_lora_noalloc(p, w, None, cr.ACT_NONE, X, A_ext, B_ext, 16)
+    assert Y2.shape == (0, 256)
+    h = cr.convrot_linear_act_pack(p, w, None, cr.ACT_GELU_ERF, 256)
+    assert (h.rows, h.k) == (0, 256)
+    torch.cuda.synchronize()
+
+
 @pytest.mark.parametrize("act", [cr.ACT_GELU_ERF, cr.ACT_GELU_TANH], ids=["gelu_erf", "gelu_tanh"])
 @pytest.mark.parametrize("codes", GEMM_CODES, ids=GEMM_IDS)
 @pytest.mark.parametrize("m,n,k", [(200, 300, 640), (64, 1000, 256), (300, 512, 1024)])
